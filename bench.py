@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 tensor-core GEMM C = epilogue(A . B).
+
+One step = one C = epilogue(A . B) call over the workload's synthetic,
+seeded inputs, already resident in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline] [--no-secondary]
+
+Default workload: square8192_bf16 (bf16 M=N=K=8192, bf16 output), the
+tensor-core roofline case.  Other workloads: see gemm_inputs.WORKLOADS.
+
+Timing: W untimed warm-up steps; then K steps bracketed by a barrier and a
+device synchronisation; each step's GEMM is timed with CUDA events on the
+launching stream, and a 256 MiB buffer is written between steps (outside
+the events) so every step starts with a cold L2.  `value` is the whole-job
+throughput: total FLOPs of all ranks / max-over-ranks of the summed event
+time.  With N > 1 every rank runs an independent replica (the path has no
+exchange step; "weak" scaling).
+
+`--impl reference` times the CPU oracle (the plain fp64 triple loop) on the
+host cores, on a bounded row-block sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gemm_inputs  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "GEMM TFLOP/s and % of GB300 dense fp16/bf16 peak (HBM GB/s for skinny-K)"
+DEFAULT_WORKLOAD = "square8192_bf16"
+HBM_BOUND = {"swin4k_proj_f16"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gemm_inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg (profiling runs)")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other-workload summary")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_core_gemm_tma_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = kernel_source_hash()
+    with open(p) as f:
+        for line in f:
+            parts = line.split("#")[0].split()
+            if len(parts) >= 3 and parts[0] == workload and parts[1] == cur:
+                return int(float(parts[2]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sg_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples under load: the upper part of the clock distribution
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def device_inputs(w, device):
+    import torch
+    a, b, bias = w.a_bits(), w.b_bits(), w.bias()
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w.in_dtype]
+    A = torch.from_numpy(a.view(np.int16)).view(tdt)
+    B = torch.from_numpy(b.view(np.int16)).view(tdt)
+    bias_t = None if bias is None else torch.from_numpy(bias.copy())
+    return A, B, bias_t
+
+
+def out_torch_dtype(w):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out_dtype]
+
+
+def time_steps(call, steps, stream, flush):
+    """Per-step CUDA-event durations (ms) of `call`, with an L2 flush between."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in evs:
+        flush()
+        s.record(stream)
+        call()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def cpu_oracle_sample(w, target_s=12.0, a=None, b=None, bias=None):
+    """Time the oracle (as it stands) on a row-block sample of the workload:
+    returns (seconds, rows, flops, threads)."""
+    import oracle
+    a = w.a_bits() if a is None else a
+    b = w.b_bits() if b is None else b
+    bias = w.bias() if bias is None else bias
+    threads = os.cpu_count() or 1
+    rows = min(w.M, max(threads, 16))
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or rows >= w.M:
+            break
+        rows = min(w.M, max(rows * 2, int(rows * (target_s / 2) / max(dt, 1e-3))))
+    return dt, rows, 2.0 * rows * w.N * w.K, threads
+
+
+def run_reference(args, w, rank, world):
+    """The oracle arm: rank 0 only, on the host cores."""
+    if rank != 0:
+        return
+    a, b, bias = w.a_bits(), w.b_bits(), w.bias()
+    # size one step's sample from a calibration run
+    _, rows, _, threads = cpu_oracle_sample(w, target_s=4.0, a=a, b=b, bias=bias)
+    import oracle
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    flops = 2.0 * rows * w.N * w.K
+    tot = sum(times)
+    value = flops * len(times) / tot / 1e12
+    sample = f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product per step ({rows * w.N} outputs)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, None),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, plan):
+    c = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype, "out_dtype": w.out_dtype,
+         "epilogue": w.epilogue, "accumulate": "f32", "layout": "A, B, C row-major, dense",
+         "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+         "description": w.description}
+    if plan:
+        c["tile"] = f"{plan['block_m']}x{plan['block_n']}x{plan['block_k']}"
+        c["stages"] = plan["stages"]
+        c["grid"] = plan["grid"]
+    return c
+
+
+def measure(sg, w, device, stream, steps, warmup, stages, inputs=None):
+    import torch
+    A_h, B_h, bias_h = inputs if inputs is not None else device_inputs(w, device)
+    A = A_h.to(device)
+    B = B_h.to(device)
+    bias = None if bias_h is None else bias_h.to(device)
+    C = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), device=device)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def call():
+        sg.stage_gemm(A, B, epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush()
+            call()
+        torch.cuda.synchronize()
+        times = time_steps(call, steps, stream, flush)
+    st = sg.device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+    return times, (A_h, B_h, bias_h), (A, B, bias, C)
+
+
+def measure_e2e(sg, w, host_inputs, device, stream, steps, stages):
+    """The same metric through the host-buffer API: pinned A, B (bias) copied
+    in, C copied out, every step, timed with events on the stream."""
+    import torch
+    A_h, B_h, bias_h = host_inputs
+    A_p = A_h.pin_memory()
+    B_p = B_h.pin_memory()
+    bias_p = None if bias_h is None else bias_h.pin_memory()
+    out_h = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), pin_memory=True)
+
+    def call():
+        sg.stage_gemm_host(A_p, B_p, out_dtype=out_h.dtype, epilogue=w.epilogue, bias_host=bias_p, stages=stages,
+                           device=device, stream=stream, out_host=out_h)
+
+    with torch.cuda.stream(stream):
+        call()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for s, e in evs:
+            s.record(stream)
+            call()
+            e.record(stream)
+        torch.cuda.synchronize()
+    ms = [s.elapsed_time(e) for s, e in evs]
+    h2d = A_p.numel() * A_p.element_size() + B_p.numel() * B_p.element_size()
+    if bias_p is not None:
+        h2d += bias_p.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+    return sum(ms) / len(ms), h2d, d2h
+
+
+def roofline_of(w, ms, peaks, traffic):
+    if w.name in HBM_BOUND:
+        achieved = w.algorithmic_bytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
+                "algorithmic_bytes_per_launch": w.algorithmic_bytes}
+    achieved = w.flops / (ms * 1e-3) / 1e12
+    # fp16 and bf16 dense tensor rates are the same (nominal ratio 1)
+    return {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+            "peak_source": f"{peaks['source']} bf16_tflops (burst; kernel timed alone)",
+            "algorithmic_flops_per_launch": w.flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    w = gemm_inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    sg.load_library()
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    clocks = ClockSampler(cvd.split(",")[local] if cvd else local)
+    host_inputs = device_inputs(w, device)
+    # warm-up + timed steps (the clock sampler runs over the timed region)
+    with clocks:
+        barrier()
+        times, host_inputs, dev_tensors = measure(sg, w, device, stream, args.steps, args.warmup, args.stages,
+                                                  inputs=host_inputs)
+        barrier()
+    sum_ms = sum(times)
+    if pg is not None:
+        t = torch.tensor([sum_ms], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        sum_ms = float(t.item())
+    ms = sum_ms / len(times)
+    value = w.flops * world * len(times) / (sum_ms * 1e-3) / 1e12
+    plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages)
+
+    e2e = None
+    if not args.no_e2e:
+        del dev_tensors
+        e2e_ms, h2d, d2h = measure_e2e(sg, w, host_inputs, device, stream, max(3, min(args.steps, 10)), args.stages)
+        e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "tensor_core_gemm_tma_gb300.stage_gemm_host (pinned host buffers)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic (seeded SplitMix64, see gemm_inputs)",
+        "config": config_of(w, plan),
+        "roofline": roofline_of(w, ms, peaks, recorded_traffic(w.name)),
+        "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
+        "gpu_launches": len(times),
+        "gpu_launches_note": "one stage_gemm kernel launch per timed step (the L2 flush between steps is a torch fill)",
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    if w.name in HBM_BOUND:
+        line["hbm_gbs"] = line["roofline"]["achieved"]
+
+    if rank == 0 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD:
+        sec = []
+        for name in ("relu4096_f16", "swin4k_proj_f16"):
+            ws = gemm_inputs.WORKLOADS[name]
+            t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0)
+            del dt
+            m2 = sum(t2) / len(t2)
+            sec.append({"workload": name, "ms_per_step": m2, "TFLOP/s": ws.flops / (m2 * 1e-3) / 1e12,
+                        "roofline": roofline_of(ws, m2, peaks, recorded_traffic(name))})
+        line["secondary"] = sec
+
+    if rank == 0 and not args.no_cpu_baseline and world >= 1:
+        dt, rows, flops, threads = cpu_oracle_sample(w)
+        line["cpu_baseline"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product "
+                                          f"({rows * w.N} outputs, {dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

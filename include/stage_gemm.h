@@ -1,0 +1,163 @@
+/*
+ * stage_gemm.h -- C ABI of the GB300 (sm_103a) tensor-core GEMM
+ *
+ *     C = epilogue(A . B)
+ *
+ * A is M x K, B is K x N, C is M x N, all row-major with leading dimensions
+ * (row pitches, in elements) lda >= K, ldb >= N, ldc >= N.  A and B are both
+ * fp16 or both bf16; the product is accumulated in fp32; C is fp32, fp16 or
+ * bf16.  The operation and its rules come from these pages:
+ *
+ *   - gizml:tile, "Tile.dot": the matrix product [M,K][K,N] -> [M,N] in F32,
+ *     on matrix cores when both operands are F16 or both are BF16.
+ *   - gizml:tile, "Tile.run" (the fused example over 128 x 128 output tiles,
+ *     storing acc.relu()), "Tile.relu" and "Tile.add": the epilogues.  The
+ *     bias of SG_EPI_BIAS_RELU is one fp32 value per column, added to the
+ *     fp32 accumulator before the ReLU, as the per-column accumulator seed of
+ *     the Swin-layer epilogue notes (d4r, rrswin_enc2_epilogues.md).
+ *   - gizml:tile, "Tile.to": the single rounding of the fp32 result into the
+ *     output type is round-to-nearest-even; overflow gives +-infinity.
+ *   - gizml:tile, "In.at": operand elements past the edge of A or B (row >= M,
+ *     column >= N, k >= K, including any ld padding) are read as 0; they are
+ *     never loaded from memory.  Tolk.Stage, "operands": a gate whose index
+ *     is invalid copies 0.
+ *   - gizml:tile, "Out.put": elements of C outside M x N (including the ldc
+ *     padding columns) are not written.
+ *   - gizml:tile, "Program.stages" and Tolk.Stage (two-stage pipeline,
+ *     "depth"): `stages` blocks of operands in flight; 1 reads each trip's
+ *     blocks in turn, 2 overlaps the next trip's copy with this trip's
+ *     products, more hide longer latency.  Tolk.Stage, module overview:
+ *     staging moves values and never rounds them, so every stage count gives
+ *     bit-identical C.
+ *   - gizml:tile, "Program.fold": an empty K range leaves the initial zeros,
+ *     so K = 0 writes C = epilogue(0 [+ bias]).
+ *   - Tolk.Uniform, "Precondition": parameters that are written do not
+ *     overlap others; C must not overlap A, B or bias.
+ *
+ * Ownership: the caller owns A, B, C and bias (device memory, e.g. from
+ * PyTorch).  The library never frees caller memory.  It allocates, once per
+ * device, a 4-byte device status word and keeps host-side caches.
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t passed as
+ * void*; NULL is the legacy default stream).  Argument checks run on the
+ * host before any CUDA call.
+ *
+ * Errors: 0 on success, a negative SG_ERR_* code otherwise (sg_strerror gives
+ * its text).  A device-side wait that gives up (see SG_ERR_TIMEOUT) is
+ * reported asynchronously through sg_device_status.
+ */
+#ifndef STAGE_GEMM_H
+#define STAGE_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage types. */
+enum {
+    SG_F32 = 0,  /* IEEE binary32 (output only) */
+    SG_F16 = 1,  /* IEEE binary16 */
+    SG_BF16 = 2  /* bfloat16 */
+};
+
+/* Epilogues applied to the fp32 accumulator before the output rounding. */
+enum {
+    SG_EPI_NONE = 0,      /* C = A.B */
+    SG_EPI_RELU = 1,      /* C = max(A.B, 0) */
+    SG_EPI_BIAS_RELU = 2  /* C = max(A.B + bias[col], 0) */
+};
+
+/* Return codes. */
+enum {
+    SG_OK = 0,
+    SG_ERR_ARG = -1,     /* M, N or K < 0; ld < row length; null pointer; bias
+                            missing for SG_EPI_BIAS_RELU or given otherwise;
+                            a dimension or pitch beyond 2^31 - 1 */
+    SG_ERR_DTYPE = -2,   /* in_dtype not fp16/bf16, out_dtype not fp32/fp16/bf16,
+                            or an unknown epilogue */
+    SG_ERR_STAGES = -3,  /* stages < 0, > SG_MAX_STAGES, or does not fit in
+                            shared memory for the chosen tile */
+    SG_ERR_ALIAS = -4,   /* C overlaps A, B or bias */
+    SG_ERR_ALIGN = -5,   /* A or B base not 16-byte aligned, or lda/ldb times
+                            the element size not a multiple of 16 bytes */
+    SG_ERR_ARCH = -6,    /* the current device is not sm_103 */
+    SG_ERR_CUDA = -7,    /* a CUDA runtime/driver call or the launch failed */
+    SG_ERR_TIMEOUT = -8  /* a device-side wait gave up (reported by
+                            sg_device_status) */
+};
+
+#define SG_MAX_STAGES 8
+#define SG_VERSION 100 /* 1.0.0 */
+
+/*
+ * sg_gemm -- C[i*ldc + j] = epilogue(sum_k A[i*lda + k] * B[k*ldb + j])
+ * for 0 <= i < M, 0 <= j < N, rounded once into out_dtype.
+ *
+ *   M, N, K     problem size (>= 0).  M == 0 or N == 0 is a no-op.
+ *   A, lda      device pointer to M x K row-major in_dtype elements; lda >= K.
+ *   B, ldb      device pointer to K x N row-major in_dtype elements; ldb >= N.
+ *   C, ldc      device pointer to M x N row-major out_dtype elements; ldc >= N.
+ *   in_dtype    SG_F16 or SG_BF16 (both operands).
+ *   out_dtype   SG_F32, SG_F16 or SG_BF16.
+ *   epilogue    SG_EPI_NONE, SG_EPI_RELU or SG_EPI_BIAS_RELU.
+ *   bias        device pointer to N fp32 values, required iff BIAS_RELU.
+ *   stages      shared-memory operand slots in flight: 0 = the largest count
+ *               that fits, else 1..SG_MAX_STAGES.
+ *   stream      cudaStream_t (as void*) the work is queued on.
+ *
+ * A and B must start on a 16-byte boundary and lda, ldb must be multiples of
+ * 8 elements (TMA rule); otherwise SG_ERR_ALIGN.  C has no alignment rule:
+ * an unaligned C uses a masked element-wise store epilogue instead of TMA
+ * stores.
+ */
+int sg_gemm(int64_t M, int64_t N, int64_t K,
+            const void* A, int64_t lda,
+            const void* B, int64_t ldb,
+            void* C, int64_t ldc,
+            int in_dtype, int out_dtype, int epilogue,
+            const float* bias, int stages, void* stream);
+
+/* The launch configuration sg_gemm would use (no GPU work is queued).
+ * Needs a current CUDA device; returns the same codes as sg_gemm. */
+typedef struct {
+    int32_t block_m;       /* output tile rows (128) */
+    int32_t block_n;       /* output tile columns */
+    int32_t block_k;       /* K elements per stage (64) */
+    int32_t stages;        /* operand slots in the shared-memory ring */
+    int32_t max_stages;    /* the largest count that fits for this tile */
+    int32_t tiles;         /* output tiles */
+    int32_t grid;          /* persistent CTAs launched */
+    int32_t threads;       /* threads per CTA */
+    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t tmem_columns;  /* tensor-memory columns allocated per CTA */
+    int32_t tma_store;     /* 1: C written by TMA stores, 0: masked stores */
+    int32_t reserved[5];
+} sg_plan_info;
+
+int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,
+            int64_t ldc, const void* C, sg_plan_info* info);
+
+/* Waits for `stream`, then returns SG_ERR_TIMEOUT if any kernel of this
+ * library on the current device gave up on a wait since the last call (and
+ * clears that record), SG_ERR_CUDA if the stream reports an error, else 0. */
+int sg_device_status(void* stream);
+
+/* The bound on each device-side wait, in nanoseconds (default 2e9; the
+ * environment variable STAGE_GEMM_WAIT_LIMIT_MS overrides it at load).
+ * Applies to launches made after the call. */
+void sg_set_wait_limit_ns(uint64_t ns);
+uint64_t sg_get_wait_limit_ns(void);
+
+/* Static text for a return code. */
+const char* sg_strerror(int code);
+
+/* SG_VERSION of the built library. */
+int sg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STAGE_GEMM_H */

@@ -1,0 +1,33 @@
+/*
+ * stage_gemm_testing.h -- test-only entry points of libstage_gemm.so.
+ *
+ * Not part of the supported interface; the test suite uses them to exercise
+ * the device-side failure path without faulting, trapping or hanging a GPU.
+ */
+#ifndef STAGE_GEMM_TESTING_H
+#define STAGE_GEMM_TESTING_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Failure injection for the bounded device waits (gizml:tile lists "fail" as
+ * an effect of every call; the pages define no device-side failure
+ * mechanism, so this hook has no counterpart there).  After this call, every
+ * CTA of every later sg_gemm launch skips the TMA copy of its K chunk with
+ * index `it` (counted over the CTA's tiles).  The MMA issuer's bounded wait
+ * for that chunk then runs out, the kernel records a timeout in the device
+ * status word, every role leaves its loop, drains its own copies and MMAs,
+ * frees tensor memory and exits; sg_device_status returns SG_ERR_TIMEOUT.
+ * C is left partly unwritten.  it < 0 switches the hook off.  Returns 0.
+ */
+int sg_test_set_skip_load(int64_t it);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STAGE_GEMM_TESTING_H */

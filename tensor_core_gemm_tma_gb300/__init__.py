@@ -1,0 +1,217 @@
+"""GB300 (sm_103a) tensor-core GEMM, C = epilogue(A . B), through the C ABI of
+``libstage_gemm.so`` (declared in ``include/stage_gemm.h``).
+
+This module only marshals arguments: every step of the product runs in the
+CUDA kernels of the library.  PyTorch supplies device memory and streams.
+There is no fallback: if the library is missing, loading raises.
+
+    import torch, tensor_core_gemm_tma_gb300 as sg
+    C = sg.stage_gemm(A, B, out_dtype=torch.float16, epilogue="relu")
+
+The operation follows gizml:tile ("Tile.dot", "Tile.run", "In.at",
+"Out.put", "Tile.to", "Program.stages") and Tolk.Stage (staged operands,
+zero-filling gates, bit-identical results at every stage count).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+LIB_PATH = _build.LIB
+
+# Storage-type and epilogue codes of the C ABI.
+SG_F32, SG_F16, SG_BF16 = 0, 1, 2
+EPILOGUES = {"none": 0, "relu": 1, "bias_relu": 2}
+SG_MAX_STAGES = 8
+
+ERRORS = {
+    -1: "SG_ERR_ARG", -2: "SG_ERR_DTYPE", -3: "SG_ERR_STAGES", -4: "SG_ERR_ALIAS",
+    -5: "SG_ERR_ALIGN", -6: "SG_ERR_ARCH", -7: "SG_ERR_CUDA", -8: "SG_ERR_TIMEOUT",
+}
+
+
+class SgError(RuntimeError):
+    """A negative return code of the C ABI."""
+
+    def __init__(self, code: int, text: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {text}")
+        self.code = code
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "block_m", "block_n", "block_k", "stages", "max_stages", "tiles", "grid", "threads", "smem_bytes",
+        "tmem_columns", "tma_store")] + [("reserved", ctypes.c_int32 * 5)]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libstage_gemm.so (built by ``__graft_entry__.build()`` or
+    ``tensor_core_gemm_tma_gb300._build.build()``).  Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is not built; run __graft_entry__.build() (nvcc, sm_103a) first")
+        lib = ctypes.CDLL(p)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.sg_gemm.restype = i32
+        lib.sg_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
+        lib.sg_plan.restype = i32
+        lib.sg_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i64, vp, ctypes.POINTER(PlanInfo)]
+        lib.sg_device_status.restype = i32
+        lib.sg_device_status.argtypes = [vp]
+        lib.sg_set_wait_limit_ns.restype = None
+        lib.sg_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.sg_get_wait_limit_ns.restype = ctypes.c_uint64
+        lib.sg_get_wait_limit_ns.argtypes = []
+        lib.sg_strerror.restype = ctypes.c_char_p
+        lib.sg_strerror.argtypes = [i32]
+        lib.sg_version.restype = i32
+        lib.sg_version.argtypes = []
+        lib.sg_test_set_skip_load.restype = i32
+        lib.sg_test_set_skip_load.argtypes = [i64]
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def strerror(code: int) -> str:
+    return load_library().sg_strerror(int(code)).decode()
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise SgError(rc, strerror(rc))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(dt) -> int:
+    torch = _torch()
+    codes = {torch.float32: SG_F32, torch.float16: SG_F16, torch.bfloat16: SG_BF16}
+    if dt not in codes:
+        raise ValueError(f"unsupported dtype {dt}")
+    return codes[dt]
+
+
+def _stream_ptr(stream, device):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _row_pitch(t) -> int:
+    """Leading dimension (elements) of a 2-D tensor with unit column stride."""
+    if t.dim() != 2:
+        raise ValueError("operands must be 2-D")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError("operands must be row-major (unit stride along columns)")
+    return max(t.stride(0), t.size(1)) if t.size(0) > 1 else t.size(1)
+
+
+def gemm_raw(M: int, N: int, K: int, A_ptr: int, lda: int, B_ptr: int, ldb: int, C_ptr: int, ldc: int,
+             in_dtype: int, out_dtype: int, epilogue: int, bias_ptr: int | None, stages: int, stream_ptr: int) -> int:
+    """The C ABI call itself, on raw pointers; returns its code."""
+    return load_library().sg_gemm(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, in_dtype, out_dtype, epilogue,
+                                  bias_ptr, stages, stream_ptr)
+
+
+def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: int = 0, out=None, stream=None):
+    """C = epilogue(A @ B) on A's CUDA device, queued on ``stream`` (default:
+    the current stream).  A (M x K) and B (K x N) are row-major fp16 or bf16
+    CUDA tensors of one dtype; ``out_dtype`` is float32 (default), float16
+    or bfloat16; ``bias`` is an fp32 CUDA vector of N values for
+    ``epilogue="bias_relu"``; ``stages`` is the operand ring depth (0: the
+    largest that fits).  ``out`` may be a preallocated row-major M x N view
+    (its padding columns are never written)."""
+    torch = _torch()
+    if A.device.type != "cuda" or B.device.type != "cuda":
+        raise ValueError("A and B must be CUDA tensors")
+    if A.dtype != B.dtype:
+        raise ValueError("A and B must have the same dtype")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    elif out_dtype is not None and out.dtype != out_dtype:
+        raise ValueError("out has a different dtype from out_dtype")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be M x N")
+    if epilogue not in EPILOGUES:
+        raise ValueError(f"epilogue must be one of {sorted(EPILOGUES)}")
+    bptr = None
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.device != A.device or bias.numel() != N or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous fp32 CUDA vector of N values")
+        bptr = bias.data_ptr()
+    rc = gemm_raw(M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), out.data_ptr(),
+                  _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype), EPILOGUES[epilogue], bptr,
+                  int(stages), _stream_ptr(stream, A.device).value)
+    _check(rc)
+    return out
+
+
+def stage_gemm_host(A_host, B_host, out_dtype=None, epilogue: str = "none", bias_host=None, stages: int = 0,
+                    device=None, stream=None, out_host=None):
+    """End-to-end call on host tensors: copies A, B (and bias) to the device,
+    runs ``stage_gemm`` and copies C back into ``out_host`` (pinned host
+    memory is used for asynchronous copies).  Returns the host tensor."""
+    torch = _torch()
+    dev = torch.device(device or "cuda")
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(s):
+        A = A_host.to(dev, non_blocking=True)
+        B = B_host.to(dev, non_blocking=True)
+        bias = None if bias_host is None else bias_host.to(dev, non_blocking=True)
+        C = stage_gemm(A, B, out_dtype=out_dtype, epilogue=epilogue, bias=bias, stages=stages, stream=s)
+        if out_host is None:
+            out_host = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+        out_host.copy_(C, non_blocking=True)
+    return out_host
+
+
+def plan(M: int, N: int, K: int, in_dtype, out_dtype, epilogue: str = "none", stages: int = 0, ldc: int | None = None,
+         C_ptr: int = 0) -> dict:
+    """The launch configuration ``stage_gemm`` would use (tile, stages, grid,
+    shared memory).  Needs a CUDA device."""
+    info = PlanInfo()
+    rc = load_library().sg_plan(M, N, K, dtype_code(in_dtype), dtype_code(out_dtype), EPILOGUES[epilogue],
+                                int(stages), N if ldc is None else ldc, C_ptr, ctypes.byref(info))
+    _check(rc)
+    return info.as_dict()
+
+
+def device_status(stream=None) -> int:
+    """Synchronises ``stream`` and returns 0, or SG_ERR_TIMEOUT (-8) when a
+    kernel of the library gave up on a device-side wait since the last call."""
+    torch = _torch()
+    return load_library().sg_device_status(_stream_ptr(stream, torch.device("cuda")).value)
+
+
+def set_wait_limit_ns(ns: int):
+    load_library().sg_set_wait_limit_ns(int(ns))
+
+
+def get_wait_limit_ns() -> int:
+    return int(load_library().sg_get_wait_limit_ns())
+
+
+def version() -> int:
+    return int(load_library().sg_version())

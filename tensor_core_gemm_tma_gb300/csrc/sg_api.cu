@@ -1,0 +1,368 @@
+// sg_api.cu -- host side of the C ABI declared in include/stage_gemm.h:
+// argument checks, the launch plan (tile width, stage count, persistent grid),
+// the TMA tensor-map builder and the kernel launch.
+//
+// Every argument check runs before the first CUDA call, so a rejected call
+// never touches the device.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "sg_kernel.cuh"
+#include "stage_gemm.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kGroupM = 8;  // row blocks swept together by the tile raster
+
+struct DevState {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;   // max dynamic shared memory per block
+    int smem_per_sm = 0;
+    int major = 0, minor = 0;
+    int* status = nullptr;  // device status word (4 bytes, library-owned)
+    bool attr_done[4][3] = {};
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+uint64_t initial_wait_limit() {
+    const char* e = std::getenv("STAGE_GEMM_WAIT_LIMIT_MS");
+    if (e && *e) {
+        char* end = nullptr;
+        const double ms = std::strtod(e, &end);
+        if (end != e && ms > 0) return static_cast<uint64_t>(ms * 1e6);
+    }
+    return 2000000000ull;  // 2 s
+}
+std::atomic<uint64_t> g_wait_limit_ns{initial_wait_limit()};
+
+// Test hook (not in the public header): the next launches skip copying the
+// K chunk with this global index, so the MMA's wait for it runs out.
+std::atomic<int64_t> g_skip_load{-1};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int elem_bytes(int dt) { return dt == SG_F32 ? 4 : 2; }
+bool valid_in(int dt) { return dt == SG_F16 || dt == SG_BF16; }
+bool valid_out(int dt) { return dt == SG_F32 || dt == SG_F16 || dt == SG_BF16; }
+bool valid_epi(int e) { return e == SG_EPI_NONE || e == SG_EPI_RELU || e == SG_EPI_BIAS_RELU; }
+
+// [p, p + n) and [q, q + m) overlap (empty ranges never do)
+bool overlap(const void* p, uint64_t n, const void* q, uint64_t m) {
+    if (!p || !q || n == 0 || m == 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + m && b < a + n;
+}
+
+uint64_t span_bytes(int64_t rows, int64_t cols, int64_t ld, int esize) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return static_cast<uint64_t>((rows - 1) * ld + cols) * static_cast<uint64_t>(esize);
+}
+
+// Host-only argument checks (no CUDA calls).
+int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+               int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias, int stages) {
+    if (!valid_in(in_dtype) || !valid_out(out_dtype) || !valid_epi(epilogue)) return SG_ERR_DTYPE;
+    if (M < 0 || N < 0 || K < 0) return SG_ERR_ARG;
+    const int64_t lim = 0x7FFFFFFF;
+    if (M > lim || N > lim || K > lim || lda > lim || ldb > lim || ldc > lim) return SG_ERR_ARG;
+    if (stages < 0 || stages > SG_MAX_STAGES) return SG_ERR_STAGES;
+    if ((epilogue == SG_EPI_BIAS_RELU) != (bias != nullptr)) return SG_ERR_ARG;
+    if (M == 0 || N == 0) return SG_OK;
+    if (!C || ldc < N) return SG_ERR_ARG;
+    if (K > 0 && (!A || !B || lda < K || ldb < N)) return SG_ERR_ARG;
+    if (cdiv(M, sg::BM) * cdiv(N, 64) > lim) return SG_ERR_ARG;
+    const uint64_t c_span = span_bytes(M, N, ldc, elem_bytes(out_dtype));
+    if (K > 0) {
+        if (overlap(C, c_span, A, span_bytes(M, K, lda, 2)) || overlap(C, c_span, B, span_bytes(K, N, ldb, 2)))
+            return SG_ERR_ALIAS;
+    }
+    if (bias && overlap(C, c_span, bias, static_cast<uint64_t>(N) * 4)) return SG_ERR_ALIAS;
+    if (K > 0) {
+        if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15)) return SG_ERR_ALIGN;
+        // a single row has no pitch to align
+        if ((M > 1 && (lda * 2) % 16) || (K > 1 && (ldb * 2) % 16)) return SG_ERR_ALIGN;
+    }
+    return SG_OK;
+}
+
+int ensure_encode_fn() {
+    if (g_encode) return SG_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return SG_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return SG_OK;
+}
+
+// Per-device set-up, once: properties, the status word, the encoder.
+int device_state(DevState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState& st = g_dev[dev];
+    if (!st.ready) {
+        if (cudaDeviceGetAttribute(&st.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return SG_ERR_CUDA;
+        if (st.major != 10 || st.minor != 3) return SG_ERR_ARCH;
+        if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+                cudaSuccess)
+            return SG_ERR_CUDA;
+        if (int rc = ensure_encode_fn(); rc != SG_OK) return rc;
+        if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return SG_ERR_CUDA;
+        if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return SG_ERR_CUDA;
+        st.ready = true;
+    }
+    *out = &st;
+    return SG_OK;
+}
+
+struct Plan {
+    int bn = 128;
+    int stages = 0, max_stages = 0;
+    int64_t m_blocks = 0, n_blocks = 0, tiles = 0, k_chunks = 0;
+    int grid = 0;
+    int smem = 0;
+    int tmem_cols = 0;
+    int tma_store = 0;
+};
+
+template <int BN>
+int layout_smem(int stages) { return sg::Layout<BN>::smem_bytes(stages); }
+
+int smem_for(int bn, int stages) {
+    switch (bn) {
+        case 128: return layout_smem<128>(stages);
+        case 256: return layout_smem<256>(stages);
+        default: return -1;
+    }
+}
+
+int tmem_cols_for(int bn) { return bn == 256 ? sg::Layout<256>::TMEM_COLS : sg::Layout<128>::TMEM_COLS; }
+
+int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype, const void* C, int64_t ldc,
+              int stages, Plan* pl) {
+    pl->m_blocks = cdiv(M, sg::BM);
+    // Tile width: 256 columns when it covers N as tightly as 128 and still
+    // fills every SM; otherwise 128.
+    int bn = 128;
+    if (N >= 256) {
+        const int64_t t256 = pl->m_blocks * cdiv(N, 256);
+        const double eff256 = static_cast<double>(N) / (cdiv(N, 256) * 256.0);
+        const double eff128 = static_cast<double>(N) / (cdiv(N, 128) * 128.0);
+        if (t256 >= st.sm_count && eff256 >= eff128) bn = 256;
+    }
+    pl->bn = bn;
+    pl->n_blocks = cdiv(N, bn);
+    pl->tiles = pl->m_blocks * pl->n_blocks;
+    pl->k_chunks = cdiv(K, sg::BK);
+    int maxs = 0;
+    for (int s = 1; s <= SG_MAX_STAGES; ++s)
+        if (smem_for(bn, s) <= st.smem_optin) maxs = s;
+    pl->max_stages = maxs;
+    if (maxs == 0) return SG_ERR_STAGES;
+    if (stages == 0) stages = maxs;
+    if (stages > maxs) return SG_ERR_STAGES;
+    pl->stages = stages;
+    pl->smem = smem_for(bn, stages);
+    pl->tmem_cols = tmem_cols_for(bn);
+    // Two CTAs on one SM would each hold half the tensor memory or wait for
+    // it; keep one persistent CTA per SM by asking for more than half of the
+    // SM's shared memory.
+    if (pl->tmem_cols > 256 && pl->smem <= st.smem_per_sm / 2) pl->smem = st.smem_per_sm / 2 + 1024;
+    pl->grid = static_cast<int>(pl->tiles < st.sm_count ? pl->tiles : st.sm_count);
+    const int oes = elem_bytes(out_dtype);
+    pl->tma_store = ((reinterpret_cast<uintptr_t>(C) & 15) == 0 && (M == 1 || (ldc * oes) % 16 == 0)) ? 1 : 0;
+    return SG_OK;
+}
+
+CUtensorMapDataType tmap_dtype(int dt) {
+    switch (dt) {
+        case SG_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        case SG_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    }
+}
+
+// 2-D row-major tensor [outer][inner] with a pitch of `pitch_bytes`, copied in
+// boxes of box_inner x box_outer elements with the 128-byte swizzle.
+int encode_2d(CUtensorMap* tm, int dt, const void* ptr, int64_t inner, int64_t outer, int64_t pitch_bytes,
+              uint32_t box_inner, uint32_t box_outer) {
+    if (outer == 1) pitch_bytes = (inner * elem_bytes(dt) + 15) / 16 * 16;  // unused, but must be legal
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(tm, tmap_dtype(dt), 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SG_OK : SG_ERR_CUDA;
+}
+
+template <int BN, int OUT>
+int launch_t(DevState& st, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+             const sg::Params& prm, cudaStream_t stream) {
+    auto kern = sg::sg_gemm_kernel<BN, OUT>;
+    const int bi = BN == 128 ? 0 : 1;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!st.attr_done[bi][OUT]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, st.smem_optin) !=
+                cudaSuccess)
+                return SG_ERR_CUDA;
+            st.attr_done[bi][OUT] = true;
+        }
+    }
+    kern<<<pl.grid, sg::NUM_THREADS, pl.smem, stream>>>(ta, tb, tc, prm);
+    return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
+}
+
+template <int BN>
+int launch_bn(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
+              const CUtensorMap& tc, const sg::Params& prm, cudaStream_t stream) {
+    switch (out_dtype) {
+        case SG_F32: return launch_t<BN, SG_F32>(st, pl, ta, tb, tc, prm, stream);
+        case SG_F16: return launch_t<BN, SG_F16>(st, pl, ta, tb, tc, prm, stream);
+        default: return launch_t<BN, SG_BF16>(st, pl, ta, tb, tc, prm, stream);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+            int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias, int stages, void* stream) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    DevState* st = nullptr;
+    if ((rc = device_state(&st)) != SG_OK) return rc;
+    Plan pl;
+    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, &pl)) != SG_OK) return rc;
+
+    alignas(64) CUtensorMap ta, tb, tc;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    std::memset(&tc, 0, sizeof(tc));
+    if (K > 0) {
+        if ((rc = encode_2d(&ta, in_dtype, A, K, M, lda * 2, sg::BK, sg::BM)) != SG_OK) return rc;
+        if ((rc = encode_2d(&tb, in_dtype, B, N, K, ldb * 2, 64, sg::BK)) != SG_OK) return rc;
+    }
+    if (pl.tma_store) {
+        const int oes = elem_bytes(out_dtype);
+        if ((rc = encode_2d(&tc, out_dtype, C, N, M, ldc * oes, 128 / oes, 32)) != SG_OK) return rc;
+    }
+
+    sg::Params prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.m_blocks = static_cast<int32_t>(pl.m_blocks);
+    prm.n_blocks = static_cast<int32_t>(pl.n_blocks);
+    prm.num_tiles = static_cast<int32_t>(pl.tiles);
+    prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
+    prm.stages = pl.stages;
+    prm.group_m = kGroupM;
+    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, sg::BM, pl.bn, true);
+    prm.epi = epilogue;
+    prm.tma_store = pl.tma_store;
+    prm.bias = bias;
+    prm.C = C;
+    prm.ldc = ldc;
+    prm.status = st->status;
+    prm.wait_limit_ns = g_wait_limit_ns.load();
+    prm.skip_load = g_skip_load.load();
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pl.bn == 256) return launch_bn<256>(*st, out_dtype, pl, ta, tb, tc, prm, s);
+    return launch_bn<128>(*st, out_dtype, pl, ta, tb, tc, prm, s);
+}
+
+int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages, int64_t ldc,
+            const void* C, sg_plan_info* info) {
+    if (!info) return SG_ERR_ARG;
+    if (!valid_in(in_dtype) || !valid_out(out_dtype) || !valid_epi(epilogue)) return SG_ERR_DTYPE;
+    if (M < 0 || N < 0 || K < 0 || ldc < N) return SG_ERR_ARG;
+    if (stages < 0 || stages > SG_MAX_STAGES) return SG_ERR_STAGES;
+    std::memset(info, 0, sizeof(*info));
+    DevState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != SG_OK) return rc;
+    Plan pl;
+    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, &pl)) != SG_OK) return rc;
+    info->block_m = sg::BM;
+    info->block_n = pl.bn;
+    info->block_k = sg::BK;
+    info->stages = pl.stages;
+    info->max_stages = pl.max_stages;
+    info->tiles = static_cast<int32_t>(pl.tiles);
+    info->grid = pl.grid;
+    info->threads = sg::NUM_THREADS;
+    info->smem_bytes = pl.smem;
+    info->tmem_columns = pl.tmem_cols;
+    info->tma_store = pl.tma_store;
+    return SG_OK;
+}
+
+int sg_device_status(void* stream) {
+    DevState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != SG_OK) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SG_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SG_ERR_CUDA;
+    if (h != 0) {
+        if (cudaMemset(st->status, 0, sizeof(int)) != cudaSuccess) return SG_ERR_CUDA;
+        return SG_ERR_TIMEOUT;
+    }
+    return SG_OK;
+}
+
+void sg_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+uint64_t sg_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+const char* sg_strerror(int code) {
+    switch (code) {
+        case SG_OK: return "success";
+        case SG_ERR_ARG: return "invalid argument (size, leading dimension, pointer or bias)";
+        case SG_ERR_DTYPE: return "unsupported storage type or epilogue";
+        case SG_ERR_STAGES: return "stage count out of range or does not fit in shared memory";
+        case SG_ERR_ALIAS: return "C overlaps A, B or bias";
+        case SG_ERR_ALIGN: return "A/B base or leading dimension not 16-byte aligned for TMA";
+        case SG_ERR_ARCH: return "current device is not sm_103 (GB300)";
+        case SG_ERR_CUDA: return "CUDA runtime or driver error";
+        case SG_ERR_TIMEOUT: return "a device-side wait gave up";
+        default: return "unknown error code";
+    }
+}
+
+int sg_version(void) { return SG_VERSION; }
+
+// Test hook, deliberately absent from the public header: launches after this
+// call never copy the K chunk with global index `it` (-1 restores normal
+// operation), so the MMA warp's bounded wait for it runs out.
+int sg_test_set_skip_load(int64_t it) {
+    g_skip_load.store(it < 0 ? -1 : it);
+    return SG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,417 @@
+// sg_kernel.cuh -- the persistent, warp-specialised sm_103a GEMM kernel
+//
+//     C = epilogue(A . B),  A: M x K row-major, B: K x N row-major (fp16/bf16),
+//     fp32 accumulation in tensor memory, C fp32 / fp16 / bf16.
+//
+// Roles (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: copies the A tile [128 x 64] and the B tile
+//               [64 x BN] of each K chunk into slot s = chunk mod stages of
+//               a shared-memory ring, 128-byte swizzled.  Operand elements
+//               outside M, N or K are zero-filled by the copy engine: this is
+//               the "gate that copies 0 where it fails" of Tolk.Stage
+//               ("operands") and the "elements past the edge read 0" of
+//               gizml:tile ("In.at").
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma for each
+//               filled slot into a 128 x BN fp32 accumulator and frees the
+//               slot with tcgen05.commit.  Two accumulators alternate so the
+//               epilogue of one tile overlaps the main loop of the next.
+//   warps 2-5   epilogue: tcgen05.ld (each warp owns its 32-lane quarter of
+//               tensor memory), + bias, ReLU, one round-to-nearest-even
+//               conversion, 128-byte swizzled staging in shared memory and a
+//               TMA store that does not write elements outside M x N
+//               (gizml:tile, "Out.put").
+//
+// The ring generalises the two-slot pipeline of Tolk.Stage (copy chunk k+1
+// into slot (k+1) mod 2 while computing on slot k mod 2) and the `stages`
+// knob of gizml:tile ("Program.stages") to S slots; full/empty mbarriers with
+// phase bits replace the workgroup barrier.  Every stage count issues the
+// same MMAs in the same K order, so C is bit-identical for all of them
+// (Tolk.Stage: staging moves values and never rounds them).
+//
+// Each warp's loop trip counts depend only on the problem size and the tile
+// index (Tolk.Uniform: barriers and matrix multiply-accumulates run under
+// uniform loop bounds); ragged edges are handled by zero-fill, never by
+// divergent trip counts.
+//
+// Every wait on an mbarrier is bounded in time.  A wait that runs out sets a
+// CTA-wide abort flag and the device status word; the other roles see the
+// flag, leave their loops, wait (bounded) for their own copies and MMAs in
+// flight, and the CTA frees its tensor memory and exits normally.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "sg_ptx.cuh"
+#include "stage_gemm.h"
+
+namespace sg {
+
+constexpr int BM = 128;                 // tile rows = MMA M = tensor-memory lanes
+constexpr int BK = 64;                  // K elements per stage: one 128-byte swizzle row of 16-bit values
+constexpr int UMMA_K = 16;              // K per tcgen05.mma.kind::f16
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_CHUNK_BYTES = BK * 64 * 2;  // one TMA box of B: 64 K-rows x 64 N-columns
+constexpr int EPI_WARPS = 4;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int EPI_BUF_BYTES = 32 * 128;     // one warp: 32 rows x 128 bytes
+constexpr int EPI_BUFS = 2;
+constexpr int SMEM_ALIGN = 1024;            // 128-byte swizzle atoms repeat every 1024 bytes
+constexpr int BAR_AREA = 256;
+
+// Device status word values: 0 = fine; otherwise a timeout site code.
+constexpr int STATUS_TIMEOUT = 0x5400;
+constexpr int SITE_PRODUCER_EMPTY = 1, SITE_MMA_TMEM_EMPTY = 2, SITE_MMA_FULL = 3, SITE_EPI_TMEM_FULL = 4;
+
+template <int BN>
+struct Layout {
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
+    static constexpr int B_STAGE_BYTES = BK * BN * 2;
+    static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static __host__ __device__ constexpr int epi_offset(int stages) { return stages * STAGE_BYTES; }
+    static __host__ __device__ constexpr int bar_offset(int stages) {
+        return epi_offset(stages) + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+    }
+    // dynamic shared memory to request (with slack for aligning the base)
+    static __host__ __device__ constexpr int smem_bytes(int stages) { return bar_offset(stages) + BAR_AREA + SMEM_ALIGN; }
+};
+
+struct Params {
+    int32_t M, N, K;
+    int32_t m_blocks, n_blocks, num_tiles, k_chunks;
+    int32_t stages;
+    int32_t group_m;       // tile raster: group_m row-blocks swept together for L2 reuse
+    uint32_t idesc;        // tcgen05 instruction descriptor
+    int32_t epi;           // SG_EPI_*
+    int32_t tma_store;     // 1: TMA stores of C, 0: masked element stores
+    const float* bias;
+    void* C;
+    int64_t ldc;
+    int* status;
+    uint64_t wait_limit_ns;
+    int64_t skip_load;     // test hook: this global K-chunk index is never copied (-1: off)
+};
+
+// Linear tile index -> (row block, column block), grouped raster.
+__device__ __forceinline__ void tile_coords(int tile, const Params& p, int& mb, int& nb) {
+    const int per_group = p.group_m * p.n_blocks;
+    const int g = tile / per_group;
+    const int first_m = g * p.group_m;
+    const int gsize = min(p.m_blocks - first_m, p.group_m);
+    const int r = tile - g * per_group;
+    mb = first_m + r % gsize;
+    nb = r / gsize;
+}
+
+// Wait for phase `parity` of `bar`, giving up after `limit` ns or when another
+// role has aborted.  A give-up by this wait records `site` in the status word.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          uint64_t limit, int site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit) {
+            *abort_flag = 1;
+            atomicCAS(status, 0, STATUS_TIMEOUT | site);
+            __threadfence();
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used to drain a role's own
+// asynchronous work before the CTA exits.
+__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit) return false;
+    }
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (OUT == SG_F16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_one(void* C, int64_t idx, float v) {
+    if constexpr (OUT == SG_F32) {
+        static_cast<float*>(C)[idx] = v;
+    } else if constexpr (OUT == SG_F16) {
+        static_cast<__half*>(C)[idx] = __float2half_rn(v);
+    } else {
+        static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
+    }
+}
+
+template <int BN, int OUT>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const Params p) {
+    using L = Layout<BN>;
+    constexpr int COLS = (OUT == SG_F32) ? 32 : 64;  // output columns per 128-byte staging row
+    static_assert(BN % COLS == 0, "tile width must hold whole staging rows");
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + SMEM_ALIGN - 1) & ~static_cast<uint32_t>(SMEM_ALIGN - 1);
+    uint8_t* gbase = smem_raw + (base - raw);
+    const int stages = p.stages;
+
+    const uint32_t bar0 = base + L::bar_offset(stages);
+    // barrier slots: full[0..7], empty[8..15], tmem_full[16..17], tmem_empty[18..19], drain[20]
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (SG_MAX_STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * SG_MAX_STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::bar_offset(stages) + 8 * (2 * SG_MAX_STAGES + 5));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), EPI_WARPS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        if (p.k_chunks > 0) {
+            prefetch_tmap(&tmA);
+            prefetch_tmap(&tmB);
+        }
+        if (p.tma_store) prefetch_tmap(&tmC);
+    }
+    __syncwarp();  // reconverge before the warp-collective (.sync.aligned) instructions below
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0 && p.k_chunks > 0) {
+            uint32_t slot = 0, phase = 0;
+            uint32_t issued = 0, last_parity = 0;  // per slot: ever filled, parity of its last fill
+            int64_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, p, mb, nb);
+                for (int kc = 0; kc < p.k_chunks; ++kc, ++it) {
+                    if (!wait_bounded(empty_bar(slot), phase ^ 1u, abort_flag, p.status, p.wait_limit_ns,
+                                      SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it != p.skip_load) {
+                        const uint32_t sa = base + slot * L::STAGE_BYTES;
+                        mbar_arrive_expect_tx(full_bar(slot), L::STAGE_BYTES);
+                        tma_load_2d(sa, &tmA, full_bar(slot), kc * BK, mb * BM);
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(sa + A_STAGE_BYTES + j * B_CHUNK_BYTES, &tmB, full_bar(slot), nb * BN + j * 64,
+                                        kc * BK);
+                        issued |= 1u << slot;
+                        last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
+                    }
+                    if (++slot == static_cast<uint32_t>(stages)) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // the CTA is leaving early: let this warp's copies land first
+                for (int s = 0; s < stages; ++s)
+                    if ((issued >> s) & 1u) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0 && p.k_chunks > 0) {
+            uint32_t slot = 0, phase = 0;
+            bool ok = true;
+            int lt = 0;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++lt) {
+                const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
+                if (!wait_bounded(tempty_bar(ab), aph ^ 1u, abort_flag, p.status, p.wait_limit_ns,
+                                  SITE_MMA_TMEM_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + ab * BN;
+                for (int kc = 0; kc < p.k_chunks; ++kc) {
+                    if (!wait_bounded(full_bar(slot), phase, abort_flag, p.status, p.wait_limit_ns, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + slot * L::STAGE_BYTES;
+                    // A: K-major, 8-row groups 1024 B apart.  B: MN-major, 8-K-row
+                    // groups 1024 B apart, 64-column blocks one TMA box apart.
+                    const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
+                    const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE_BYTES, B_CHUNK_BYTES, 1024);
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
+                        umma_f16(d_tmem, a_desc + ((k * UMMA_K * 2) >> 4), b_desc + ((k * UMMA_K * 128) >> 4),
+                                 p.idesc, (kc | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(slot));
+                    if (++slot == static_cast<uint32_t>(stages)) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(ab));
+            }
+            // every MMA of this CTA has completed before tensor memory is released
+            umma_commit(drain_bar);
+            wait_drain(drain_bar, 0, p.wait_limit_ns);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
+        const uint32_t stage0 = base + L::epi_offset(stages) + (warp - 2) * EPI_BUFS * EPI_BUF_BYTES;
+        uint32_t buf_i = 0;
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
+            const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
+            int mb, nb;
+            tile_coords(tile, p, mb, nb);
+            if (p.k_chunks > 0) {
+                const bool w = wait_bounded(tfull_bar(ab), aph, abort_flag, p.status, p.wait_limit_ns,
+                                            SITE_EPI_TMEM_FULL);
+                if (!__all_sync(0xffffffffu, w)) break;
+                tc_fence_after();
+            }
+            const int row0 = mb * BM + q * 32;
+            const int row = row0 + lane;
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += COLS) {
+                const int col0 = nb * BN + c;
+                float v[COLS];
+                if (p.k_chunks > 0) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(t_row + c, r);
+                    if constexpr (COLS == 64) {
+                        uint32_t r2[32];
+                        tmem_ld_32x32b_x32(t_row + c + 32, r2);
+                        tmem_wait_ld_dep(r);
+                        tmem_wait_ld_dep(r2);  // already complete; orders the uses of r2
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r2[i]);
+                    } else {
+                        tmem_wait_ld_dep(r);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < COLS; ++i) v[i] = 0.0f;
+                }
+                if (p.epi == SG_EPI_BIAS_RELU) {
+#pragma unroll
+                    for (int i = 0; i < COLS; ++i) {
+                        const int col = col0 + i;
+                        v[i] += (col < p.N) ? __ldg(p.bias + col) : 0.0f;
+                    }
+                }
+                if (p.epi != SG_EPI_NONE) {
+#pragma unroll
+                    for (int i = 0; i < COLS; ++i) v[i] = (v[i] <= 0.0f) ? 0.0f : v[i];
+                }
+                if (p.tma_store) {
+                    if (row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
+                        const uint32_t buf = stage0 + (buf_i & 1u) * EPI_BUF_BYTES;
+                        if (lane == 0) bulk_wait_group_read<1>();  // the store that used this buffer has read it
+                        __syncwarp();
+                        const uint32_t rowaddr = buf + lane * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint32_t w0, w1, w2, w3;
+                            if constexpr (OUT == SG_F32) {
+                                w0 = __float_as_uint(v[4 * j + 0]);
+                                w1 = __float_as_uint(v[4 * j + 1]);
+                                w2 = __float_as_uint(v[4 * j + 2]);
+                                w3 = __float_as_uint(v[4 * j + 3]);
+                            } else {
+                                w0 = pack2<OUT>(v[8 * j + 0], v[8 * j + 1]);
+                                w1 = pack2<OUT>(v[8 * j + 2], v[8 * j + 3]);
+                                w2 = pack2<OUT>(v[8 * j + 4], v[8 * j + 5]);
+                                w3 = pack2<OUT>(v[8 * j + 6], v[8 * j + 7]);
+                            }
+                            // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r mod 8)
+                            st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), w0, w1, w2, w3);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, buf, col0, row0);
+                            bulk_commit_group();
+                        }
+                        ++buf_i;
+                    }
+                } else if (row < p.M) {
+#pragma unroll
+                    for (int i = 0; i < COLS; ++i) {
+                        const int col = col0 + i;
+                        if (col < p.N) store_one<OUT>(p.C, static_cast<int64_t>(row) * p.ldc + col, v[i]);
+                    }
+                }
+                __syncwarp();  // the next tcgen05.ld is warp-collective
+            }
+            if (p.k_chunks > 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(ab));
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    __syncwarp();  // lanes that skipped a lane-0 role wait for it here
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+}  // namespace sg

@@ -1,0 +1,118 @@
+"""The C ABI library without a GPU: it builds, loads, exports every function
+the headers declare, and rejects bad arguments on the host before any CUDA
+call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("stage_gemm.h", "stage_gemm_testing.h")]
+
+
+@pytest.fixture(scope="module")
+def sg():
+    from tensor_core_gemm_tma_gb300 import _build
+    _build.build()
+    import tensor_core_gemm_tma_gb300 as mod
+    mod.load_library()
+    return mod
+
+
+def _declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(sg_[a-z_0-9]+)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_headers_declare_the_api():
+    names = _declared_functions()
+    for n in ("sg_gemm", "sg_plan", "sg_device_status", "sg_strerror", "sg_version", "sg_set_wait_limit_ns",
+              "sg_get_wait_limit_ns", "sg_test_set_skip_load"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(sg):
+    lib = ctypes.CDLL(sg.LIB_PATH)
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strerror(sg):
+    assert sg.version() == 100
+    for code in range(0, -9, -1):
+        txt = sg.strerror(code)
+        assert txt and txt != "unknown error code"
+    assert sg.strerror(-99) == "unknown error code"
+
+
+def test_header_codes_match_binding():
+    text = open(HEADERS[0]).read()
+    codes = dict(re.findall(r"(SG_ERR_[A-Z]+)\s*=\s*(-\d+)", text))
+    import tensor_core_gemm_tma_gb300 as mod
+    for v, name in mod.ERRORS.items():
+        assert int(codes[name]) == v
+    assert re.search(r"SG_F16 = 1", text) and re.search(r"SG_BF16 = 2", text) and re.search(r"SG_F32 = 0", text)
+    assert re.search(r"#define SG_MAX_STAGES 8", text)
+
+
+# Pointers below are never dereferenced: every call is rejected on the host.
+P16 = 0x10000      # 16-byte aligned fake addresses
+P16B = 0x900000
+PC = 0x4000000
+
+
+def call(sg, M=64, N=64, K=64, A=P16, lda=None, B=P16B, ldb=None, C=PC, ldc=None, ind=1, outd=0, epi=0,
+         bias=None, stages=0):
+    return sg.gemm_raw(M, N, K, A, K if lda is None else lda, B, N if ldb is None else ldb, C,
+                       N if ldc is None else ldc, ind, outd, epi, bias, stages, None)
+
+
+def test_empty_problem_is_a_noop(sg):
+    assert call(sg, M=0) == 0
+    assert call(sg, N=0) == 0
+    assert call(sg, M=0, N=0, K=0, A=None, B=None, C=None) == 0
+
+
+def test_rejects_bad_sizes_and_pitches(sg):
+    assert call(sg, M=-1) == -1
+    assert call(sg, K=-5) == -1
+    assert call(sg, lda=63) == -1
+    assert call(sg, ldb=10) == -1
+    assert call(sg, ldc=63) == -1
+    assert call(sg, M=1 << 31) == -1
+    assert call(sg, A=None) == -1
+    assert call(sg, C=None) == -1
+
+
+def test_rejects_bad_types_and_epilogues(sg):
+    assert call(sg, ind=0) == -2           # fp32 operands are not supported
+    assert call(sg, outd=7) == -2
+    assert call(sg, epi=3) == -2
+    assert call(sg, epi=2, bias=None) == -1
+    assert call(sg, epi=0, bias=0x7000000) == -1
+
+
+def test_rejects_bad_stage_counts(sg):
+    assert call(sg, stages=-1) == -3
+    assert call(sg, stages=9) == -3
+
+
+def test_rejects_aliasing(sg):
+    # C overlapping A, B or bias (Tolk.Uniform precondition: written
+    # parameters do not overlap the others)
+    assert call(sg, C=P16 + 64) == -4
+    assert call(sg, C=P16B) == -4
+    assert call(sg, epi=2, bias=PC + 128) == -4
+
+
+def test_rejects_tma_misalignment(sg):
+    assert call(sg, A=P16 + 2) == -5
+    assert call(sg, B=P16B + 8) == -5
+    assert call(sg, K=60, lda=60) == -5     # 120-byte pitch
+    assert call(sg, N=100, ldb=100, ldc=100) == -5

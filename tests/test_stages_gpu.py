@@ -1,0 +1,74 @@
+"""Staging moves values and never rounds them (Tolk.Stage, module overview;
+gizml:tile, "tune": every configuration computes the same result): C is
+bit-identical for every ring depth, and repeated runs are bit-identical
+(a race on a ring slot would show up as differing bits)."""
+import numpy as np
+import pytest
+
+import gemm_inputs
+import oracle
+from parity_util import compare, run_gpu, seeded_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from tensor_core_gemm_tma_gb300 import _build
+    _build.build()
+
+
+def _plan(M, N, K, ind, outd, stages=0):
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    t = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    return sg.plan(M, N, K, t[ind], t[outd], stages=stages)
+
+
+def test_stage_counts_bit_identical_bn128():
+    w = gemm_inputs.WORKLOADS["ragged1000_f16"]
+    a, b = w.a_bits(), w.b_bits()
+    p = _plan(w.M, w.N, w.K, "f16", "f32")
+    assert p["block_n"] == 128 and p["max_stages"] >= 4
+    outs = {s: run_gpu(a, b, w.M, w.N, w.K, "f16", "f32", stages=s) for s in range(1, p["max_stages"] + 1)}
+    outs[0] = run_gpu(a, b, w.M, w.N, w.K, "f16", "f32", stages=0)
+    for s, o in outs.items():
+        assert np.array_equal(o, outs[1]), f"stages={s} differs from stages=1"
+    ref, _, S = oracle.gemm(a, b, "f16", "f32")
+    compare(outs[1], ref, S, "f32", "stages")
+
+
+def test_stage_counts_bit_identical_bn256():
+    M, N, K = 2560, 2048, 520          # enough tiles for the 256-wide tile; ragged K
+    a, b = seeded_case(M, N, K, "bf16", seed=21, dist=("uniform", -1.0, 1.0))
+    p = _plan(M, N, K, "bf16", "bf16")
+    assert p["block_n"] == 256 and p["max_stages"] >= 4
+    outs = [run_gpu(a, b, M, N, K, "bf16", "bf16", stages=s) for s in (1, 2, 3, 4)]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    rng = np.random.default_rng(3)
+    rows = np.concatenate([rng.integers(0, M, 3000), np.full(N, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, 3000), np.arange(N)])
+    ref, _, S = oracle.gemm_at(a, b, rows, cols, "bf16", "bf16")
+    compare(outs[0][rows, cols], ref, S, "bf16", "bn256")
+
+
+def test_repeated_runs_bit_identical():
+    M, N, K = 1536, 1280, 768
+    a, b = seeded_case(M, N, K, "f16", seed=22)
+    first = run_gpu(a, b, M, N, K, "f16", "f16", "relu")
+    for _ in range(3):
+        assert np.array_equal(run_gpu(a, b, M, N, K, "f16", "f16", "relu"), first)
+
+
+def test_stage_count_rejected_when_too_deep():
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    p = _plan(2560, 2048, 512, "bf16", "bf16")
+    if p["max_stages"] >= 8:
+        pytest.skip("every stage count fits")
+    A = torch.zeros(2560, 512, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(512, 2048, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sg.SgError) as e:
+        sg.stage_gemm(A, B, out_dtype=torch.bfloat16, stages=p["max_stages"] + 1)
+    assert e.value.code == -3
