@@ -156,6 +156,52 @@ const char* sg_strerror(int code);
 /* SG_VERSION of the built library. */
 int sg_version(void);
 
+/*
+ * sg_gemm_noalloc -- the same GEMM as sg_gemm, for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry
+ * point; it exists for the library's users, not for the method.
+ *
+ * Who needs it: code that runs where cudaMalloc is not allowed or not
+ * wanted -- inside a host memory-pool or allocator callback, under an
+ * embedding runtime that owns every device allocation (and budgets it), or
+ * in a process that must not grow its device footprint after start-up.
+ * sg_gemm allocates a 4-byte device status word on its first call on each
+ * device; this entry point never does.
+ *
+ * Scratch: the kernel's only scratch memory is that status word (written by
+ * a device-side wait that gives up).  Here it lives in a file-scope
+ * static __device__ array of SG_NOALLOC_SCRATCH_BYTES (256) bytes, which
+ * every GPU that loads the library holds until the process exits.  This
+ * kernel needs 4 bytes of it whatever M, N and K are; a need above the
+ * array's size would be rejected with SG_ERR_ARG.
+ *
+ * Set-up: the first call on a device (with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress and queries the
+ * device's attributes; make that first call before any stream capture.
+ * Later calls do no set-up.  No call allocates: no cudaMalloc, cudaFree or
+ * allocating library routine.  The caller passes inputs and outputs exactly
+ * as for sg_gemm; arguments, return codes and results are sg_gemm's.
+ *
+ * Sharing: every call uses the same array and leaves its contents behind.
+ * Each call clears the status word on `stream` before its kernel runs, so
+ * sg_gemm_noalloc_status reports the most recent call.  Calls whose kernels
+ * overlap on the GPU (on different streams, or from different threads)
+ * race on the status word: serialise them if the status matters.
+ */
+#define SG_NOALLOC_SCRATCH_BYTES 256
+int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K,
+                    const void* A, int64_t lda,
+                    const void* B, int64_t ldb,
+                    void* C, int64_t ldc,
+                    int in_dtype, int out_dtype, int epilogue,
+                    const float* bias, int stages, void* stream);
+
+/* Waits for `stream`, then returns SG_ERR_TIMEOUT if the last
+ * sg_gemm_noalloc kernel on the current device gave up on a device-side
+ * wait, SG_ERR_CUDA on a stream error, else 0.  Allocates nothing; reads the
+ * status word with a plain device-to-host copy. */
+int sg_gemm_noalloc_status(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

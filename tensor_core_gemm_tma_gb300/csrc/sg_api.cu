@@ -366,3 +366,114 @@ int sg_test_set_skip_load(int64_t it) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (sg_gemm_noalloc): the status word lives in a
+// static device array instead of library-allocated memory.
+
+static __device__ __align__(256) int sg_noalloc_scratch[SG_NOALLOC_SCRATCH_BYTES / sizeof(int)];
+
+namespace {
+
+constexpr size_t kNoallocScratchNeed = sizeof(int);  // one status word, whatever the problem size
+DevState g_noalloc_dev[kMaxDevices];
+
+// Per-device set-up for the allocation-free path: attributes, the tensor-map
+// encoder and the device address of the static scratch array.  No
+// allocation.  Runs on the first call on each device.
+int noalloc_state(DevState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState& st = g_noalloc_dev[dev];
+    if (!st.ready) {
+        if (cudaDeviceGetAttribute(&st.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return SG_ERR_CUDA;
+        if (st.major != 10 || st.minor != 3) return SG_ERR_ARCH;
+        if (cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+                cudaSuccess)
+            return SG_ERR_CUDA;
+        if (int rc = ensure_encode_fn(); rc != SG_OK) return rc;
+        // In host code the array's name is only a host-side stand-in; the
+        // kernel must be given the device address.
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, sg_noalloc_scratch) != cudaSuccess || ptr == nullptr) return SG_ERR_CUDA;
+        st.status = static_cast<int*>(ptr);
+        st.ready = true;
+    }
+    *out = &st;
+    return SG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                    int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias, int stages,
+                    void* stream) {
+    static_assert(kNoallocScratchNeed <= SG_NOALLOC_SCRATCH_BYTES, "scratch array too small");
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    if (kNoallocScratchNeed > SG_NOALLOC_SCRATCH_BYTES) return SG_ERR_ARG;  // the need is fixed; never taken
+    DevState* st = nullptr;
+    if ((rc = noalloc_state(&st)) != SG_OK) return rc;
+    Plan pl;
+    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, &pl)) != SG_OK) return rc;
+
+    alignas(64) CUtensorMap ta, tb, tc;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    std::memset(&tc, 0, sizeof(tc));
+    if (K > 0) {
+        if ((rc = encode_2d(&ta, in_dtype, A, K, M, lda * 2, sg::BK, sg::BM)) != SG_OK) return rc;
+        if ((rc = encode_2d(&tb, in_dtype, B, N, K, ldb * 2, 64, sg::BK)) != SG_OK) return rc;
+    }
+    if (pl.tma_store) {
+        const int oes = elem_bytes(out_dtype);
+        if ((rc = encode_2d(&tc, out_dtype, C, N, M, ldc * oes, 128 / oes, 32)) != SG_OK) return rc;
+    }
+
+    sg::Params prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.m_blocks = static_cast<int32_t>(pl.m_blocks);
+    prm.n_blocks = static_cast<int32_t>(pl.n_blocks);
+    prm.num_tiles = static_cast<int32_t>(pl.tiles);
+    prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
+    prm.stages = pl.stages;
+    prm.group_m = kGroupM;
+    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, sg::BM, pl.bn, true);
+    prm.epi = epilogue;
+    prm.tma_store = pl.tma_store;
+    prm.bias = bias;
+    prm.C = C;
+    prm.ldc = ldc;
+    prm.status = st->status;
+    prm.wait_limit_ns = g_wait_limit_ns.load();
+    prm.skip_load = -1;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's word: clear it for this call
+    if (cudaMemsetAsync(st->status, 0, sizeof(int), s) != cudaSuccess) return SG_ERR_CUDA;
+    if (pl.bn == 256) return launch_bn<256>(*st, out_dtype, pl, ta, tb, tc, prm, s);
+    return launch_bn<128>(*st, out_dtype, pl, ta, tb, tc, prm, s);
+}
+
+int sg_gemm_noalloc_status(void* stream) {
+    DevState* st = nullptr;
+    int rc = noalloc_state(&st);
+    if (rc != SG_OK) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SG_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SG_ERR_CUDA;
+    return h != 0 ? SG_ERR_TIMEOUT : SG_OK;
+}
+
+}  // extern "C"
