@@ -26,6 +26,27 @@ extern "C" {
  */
 int sg_test_set_skip_load(int64_t it);
 
+/*
+ * Forces the output tile width of later sg_gemm / sg_plan calls to `bn`
+ * columns (128, 192 or 256; 0 restores the planner's choice).  Every width
+ * issues the same MMAs in the same K order for each output element, so C
+ * must be bit-identical across widths (gizml:tile, "tune": every
+ * configuration computes the same result).  Returns 0, or SG_ERR_ARG for any
+ * other width.  The environment variable STAGE_GEMM_TILE_N sets the initial
+ * value when the library loads.
+ */
+int sg_test_set_tile_n(int bn);
+
+/*
+ * Forces the cluster size of later sg_gemm / sg_plan calls: 1 (every CTA
+ * copies its whole B tile) or 2 (two CTAs with vertically adjacent tiles
+ * share each B tile through TMA multicast; only for tile widths of 128 or
+ * 256); 0 restores the planner's choice.  Both issue the same MMAs in the
+ * same order, so C must be bit-identical.  Returns 0, or SG_ERR_ARG.  The
+ * environment variable STAGE_GEMM_CLUSTER sets the initial value at load.
+ */
+int sg_test_set_cluster(int cm);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,8 @@ struct DevState {
     int smem_per_sm = 0;
     int major = 0, minor = 0;
     int* status = nullptr;  // device status word (4 bytes, library-owned)
-    bool attr_done[4][3] = {};
+    bool attr_done[3][3][2] = {};  // [tile-width variant][output type][cluster variant]
+    int max_clusters[3][3][2] = {};  // co-resident clusters of each instantiation (0: not queried)
 };
 
 std::mutex g_mu;
@@ -135,6 +136,7 @@ int device_state(DevState** out) {
 
 struct Plan {
     int bn = 128;
+    int cm = 1;  // CTAs per cluster along M (B tile multicast when 2)
     int stages = 0, max_stages = 0;
     int64_t m_blocks = 0, n_blocks = 0, tiles = 0, k_chunks = 0;
     int grid = 0;
@@ -149,29 +151,62 @@ int layout_smem(int stages) { return sg::Layout<BN>::smem_bytes(stages); }
 int smem_for(int bn, int stages) {
     switch (bn) {
         case 128: return layout_smem<128>(stages);
+        case 192: return layout_smem<192>(stages);
         case 256: return layout_smem<256>(stages);
         default: return -1;
     }
 }
 
-int tmem_cols_for(int bn) { return bn == 256 ? sg::Layout<256>::TMEM_COLS : sg::Layout<128>::TMEM_COLS; }
+// Tile width forced by sg_test_set_tile_n or, at load, the environment
+// variable STAGE_GEMM_TILE_N (128, 192 or 256; 0: the planner's choice).  A
+// tuning knob only: every width sums the same products for each output
+// element in the same K order.
+int valid_bn(int x) { return (x == 128 || x == 192 || x == 256) ? x : 0; }
+std::atomic<int> g_force_bn{[] {
+    const char* e = std::getenv("STAGE_GEMM_TILE_N");
+    return e ? valid_bn(std::atoi(e)) : 0;
+}()};
+int forced_bn() { return g_force_bn.load(); }
+
+// Cluster size forced by sg_test_set_cluster or, at load, the environment
+// variable STAGE_GEMM_CLUSTER (1 or 2; 0: the planner's choice).
+std::atomic<int> g_force_cm{[] {
+    const char* e = std::getenv("STAGE_GEMM_CLUSTER");
+    const int x = e ? std::atoi(e) : 0;
+    return (x == 1 || x == 2) ? x : 0;
+}()};
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype, const void* C, int64_t ldc,
               int stages, Plan* pl) {
     pl->m_blocks = cdiv(M, sg::BM);
-    // Tile width: 256 columns when it covers N as tightly as 128 and still
-    // fills every SM; otherwise 128.
+    pl->k_chunks = cdiv(K, sg::BK);
+    // Tile width: the widest of 256 / 192 / 128 that covers N as tightly as
+    // 128 does (no more padded columns) and still gives every SM a tile.  A
+    // short K loop (<= 4 chunks) makes the epilogue the bottleneck: keep 128,
+    // whose four tensor-memory accumulators overlap it best.
     int bn = 128;
-    if (N >= 256) {
-        const int64_t t256 = pl->m_blocks * cdiv(N, 256);
-        const double eff256 = static_cast<double>(N) / (cdiv(N, 256) * 256.0);
-        const double eff128 = static_cast<double>(N) / (cdiv(N, 128) * 128.0);
-        if (t256 >= st.sm_count && eff256 >= eff128) bn = 256;
+    const double eff128 = static_cast<double>(N) / (cdiv(N, 128) * 128.0);
+    for (int cand : {256, 192}) {
+        if (pl->k_chunks <= 4) break;
+        if (N < cand) continue;
+        const double eff = static_cast<double>(N) / (cdiv(N, cand) * static_cast<double>(cand));
+        if (pl->m_blocks * cdiv(N, cand) >= st.sm_count && eff >= eff128) {
+            bn = cand;
+            break;
+        }
     }
+    if (forced_bn()) bn = forced_bn();
     pl->bn = bn;
     pl->n_blocks = cdiv(N, bn);
-    pl->tiles = pl->m_blocks * pl->n_blocks;
-    pl->k_chunks = cdiv(K, sg::BK);
+    // Pairs of CTAs share each B tile (multicast) when the problem is large
+    // and the K loop long enough for operand traffic to matter.
+    int cm = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pl->m_blocks * pl->n_blocks >= st.sm_count &&
+              (bn / 64) % 2 == 0)
+                 ? 2
+                 : 1;
+    if (const int f = g_force_cm.load(); f == 1 || (f == 2 && (bn / 64) % 2 == 0)) cm = f;
+    pl->cm = cm;
+    pl->tiles = cdiv(pl->m_blocks, cm) * pl->n_blocks;  // cluster tiles
     int maxs = 0;
     for (int s = 1; s <= SG_MAX_STAGES; ++s)
         if (smem_for(bn, s) <= st.smem_optin) maxs = s;
@@ -181,12 +216,13 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
     if (stages > maxs) return SG_ERR_STAGES;
     pl->stages = stages;
     pl->smem = smem_for(bn, stages);
-    pl->tmem_cols = tmem_cols_for(bn);
+    pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for
     // it; keep one persistent CTA per SM by asking for more than half of the
     // SM's shared memory.
     if (pl->tmem_cols > 256 && pl->smem <= st.smem_per_sm / 2) pl->smem = st.smem_per_sm / 2 + 1024;
-    pl->grid = static_cast<int>(pl->tiles < st.sm_count ? pl->tiles : st.sm_count);
+    const int64_t clusters = st.sm_count / cm;
+    pl->grid = static_cast<int>((pl->tiles < clusters ? pl->tiles : clusters) * cm);
     const int oes = elem_bytes(out_dtype);
     pl->tma_store = ((reinterpret_cast<uintptr_t>(C) & 15) == 0 && (M == 1 || (ldc * oes) % 16 == 0)) ? 1 : 0;
     return SG_OK;
@@ -215,31 +251,71 @@ int encode_2d(CUtensorMap* tm, int dt, const void* ptr, int64_t inner, int64_t o
     return r == CUDA_SUCCESS ? SG_OK : SG_ERR_CUDA;
 }
 
-template <int BN, int OUT>
+template <int BN, int OUT, int CM>
 int launch_t(DevState& st, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
              const sg::Params& prm, cudaStream_t stream) {
-    auto kern = sg::sg_gemm_kernel<BN, OUT>;
-    const int bi = BN == 128 ? 0 : 1;
+    auto kern = sg::sg_gemm_kernel<BN, OUT, CM>;
+    const int bi = BN == 128 ? 0 : BN == 192 ? 1 : 2;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(sg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int grid = pl.grid;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!st.attr_done[bi][OUT]) {
+        if (!st.attr_done[bi][OUT][CM - 1]) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, st.smem_optin) !=
                 cudaSuccess)
                 return SG_ERR_CUDA;
-            st.attr_done[bi][OUT] = true;
+            st.attr_done[bi][OUT][CM - 1] = true;
+        }
+        if (CM > 1) {
+            int& mc = st.max_clusters[bi][OUT][CM - 1];
+            if (mc == 0) {
+                cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
+                int n = 0;
+                mc = (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) ? n : -1;
+                cudaGetLastError();  // a failed query is not a launch error
+            }
+            // a persistent grid larger than what can be co-resident only adds a tail
+            if (mc > 0 && grid > mc * CM) grid = mc * CM;
         }
     }
-    kern<<<pl.grid, sg::NUM_THREADS, pl.smem, stream>>>(ta, tb, tc, prm);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return SG_ERR_CUDA;
+    }
     return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
 }
 
-template <int BN>
+template <int BN, int CM>
 int launch_bn(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
               const CUtensorMap& tc, const sg::Params& prm, cudaStream_t stream) {
     switch (out_dtype) {
-        case SG_F32: return launch_t<BN, SG_F32>(st, pl, ta, tb, tc, prm, stream);
-        case SG_F16: return launch_t<BN, SG_F16>(st, pl, ta, tb, tc, prm, stream);
-        default: return launch_t<BN, SG_BF16>(st, pl, ta, tb, tc, prm, stream);
+        case SG_F32: return launch_t<BN, SG_F32, CM>(st, pl, ta, tb, tc, prm, stream);
+        case SG_F16: return launch_t<BN, SG_F16, CM>(st, pl, ta, tb, tc, prm, stream);
+        default: return launch_t<BN, SG_BF16, CM>(st, pl, ta, tb, tc, prm, stream);
+    }
+}
+
+int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
+                const CUtensorMap& tc, const sg::Params& prm, cudaStream_t stream) {
+    if (pl.cm == 2) {
+        if (pl.bn == 256) return launch_bn<256, 2>(st, out_dtype, pl, ta, tb, tc, prm, stream);
+        return launch_bn<128, 2>(st, out_dtype, pl, ta, tb, tc, prm, stream);
+    }
+    switch (pl.bn) {
+        case 256: return launch_bn<256, 1>(st, out_dtype, pl, ta, tb, tc, prm, stream);
+        case 192: return launch_bn<192, 1>(st, out_dtype, pl, ta, tb, tc, prm, stream);
+        default: return launch_bn<128, 1>(st, out_dtype, pl, ta, tb, tc, prm, stream);
     }
 }
 
@@ -292,8 +368,7 @@ int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
     prm.skip_load = g_skip_load.load();
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pl.bn == 256) return launch_bn<256>(*st, out_dtype, pl, ta, tb, tc, prm, s);
-    return launch_bn<128>(*st, out_dtype, pl, ta, tb, tc, prm, s);
+    return launch_plan(*st, out_dtype, pl, ta, tb, tc, prm, s);
 }
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages, int64_t ldc,
@@ -319,6 +394,7 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
     info->smem_bytes = pl.smem;
     info->tmem_columns = pl.tmem_cols;
     info->tma_store = pl.tma_store;
+    info->cluster_m = pl.cm;
     return SG_OK;
 }
 
@@ -362,6 +438,18 @@ int sg_version(void) { return SG_VERSION; }
 // operation), so the MMA warp's bounded wait for it runs out.
 int sg_test_set_skip_load(int64_t it) {
     g_skip_load.store(it < 0 ? -1 : it);
+    return SG_OK;
+}
+
+int sg_test_set_tile_n(int bn) {
+    if (bn != 0 && !valid_bn(bn)) return SG_ERR_ARG;
+    g_force_bn.store(bn);
+    return SG_OK;
+}
+
+int sg_test_set_cluster(int cm) {
+    if (cm < 0 || cm > 2) return SG_ERR_ARG;
+    g_force_cm.store(cm);
     return SG_OK;
 }
 
@@ -462,8 +550,7 @@ int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's word: clear it for this call
     if (cudaMemsetAsync(st->status, 0, sizeof(int), s) != cudaSuccess) return SG_ERR_CUDA;
-    if (pl.bn == 256) return launch_bn<256>(*st, out_dtype, pl, ta, tb, tc, prm, s);
-    return launch_bn<128>(*st, out_dtype, pl, ta, tb, tc, prm, s);
+    return launch_plan(*st, out_dtype, pl, ta, tb, tc, prm, s);
 }
 
 int sg_gemm_noalloc_status(void* stream) {

@@ -3,7 +3,7 @@
 //     C = epilogue(A . B),  A: M x K row-major, B: K x N row-major (fp16/bf16),
 //     fp32 accumulation in tensor memory, C fp32 / fp16 / bf16.
 //
-// Roles (one CTA per SM, 192 threads):
+// Roles (one CTA per SM, 320 threads):
 //   warp 0      TMA producer: copies the A tile [128 x 64] and the B tile
 //               [64 x BN] of each K chunk into slot s = chunk mod stages of
 //               a shared-memory ring, 128-byte swizzled.  Operand elements
@@ -13,13 +13,22 @@
 //               gizml:tile ("In.at").
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma for each
 //               filled slot into a 128 x BN fp32 accumulator and frees the
-//               slot with tcgen05.commit.  Two accumulators alternate so the
-//               epilogue of one tile overlaps the main loop of the next.
-//   warps 2-5   epilogue: tcgen05.ld (each warp owns its 32-lane quarter of
-//               tensor memory), + bias, ReLU, one round-to-nearest-even
+//               slot with tcgen05.commit.  512 / BN accumulators rotate, so
+//               the epilogue of earlier tiles overlaps the main loop of the
+//               next.
+//   warps 2-9   epilogue: two warps per 32-lane quarter of tensor memory
+//               (a warp may only read the quarter given by its index mod 4),
+//               each taking every other 128-byte-wide column chunk:
+//               tcgen05.ld, + bias, ReLU, one round-to-nearest-even
 //               conversion, 128-byte swizzled staging in shared memory and a
 //               TMA store that does not write elements outside M x N
 //               (gizml:tile, "Out.put").
+//
+// Clusters (CM = 2): the two CTAs of a cluster own vertically adjacent tiles
+// with the same column block, so they need the same B tile.  Each copies half
+// of its 64-column boxes and multicasts them to both CTAs' rings, halving the
+// B traffic from L2; a ring slot is free only when both CTAs' MMAs have read
+// it (the empty barrier counts one commit from each CTA).
 //
 // The ring generalises the two-slot pipeline of Tolk.Stage (copy chunk k+1
 // into slot (k+1) mod 2 while computing on slot k mod 2) and the `stages`
@@ -53,10 +62,11 @@ constexpr int BK = 64;                  // K elements per stage: one 128-byte sw
 constexpr int UMMA_K = 16;              // K per tcgen05.mma.kind::f16
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int B_CHUNK_BYTES = BK * 64 * 2;  // one TMA box of B: 64 K-rows x 64 N-columns
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int EPI_BUF_BYTES = 32 * 128;     // one warp: 32 rows x 128 bytes
-constexpr int EPI_BUFS = 2;
+constexpr int EPI_BUF_BYTES = 32 * 128;     // one warp's staging buffer: 32 rows x 128 bytes
+constexpr int TMEM_COLS = 512;              // the whole tensor memory of the SM
+constexpr int MAX_ACC = 4;                  // accumulators in flight (512 / 128)
 constexpr int SMEM_ALIGN = 1024;            // 128-byte swizzle atoms repeat every 1024 bytes
 constexpr int BAR_AREA = 256;
 
@@ -69,10 +79,10 @@ struct Layout {
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
     static constexpr int B_STAGE_BYTES = BK * BN * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static constexpr int ACC = (TMEM_COLS / BN) < MAX_ACC ? (TMEM_COLS / BN) : MAX_ACC;
     static __host__ __device__ constexpr int epi_offset(int stages) { return stages * STAGE_BYTES; }
     static __host__ __device__ constexpr int bar_offset(int stages) {
-        return epi_offset(stages) + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+        return epi_offset(stages) + EPI_WARPS * EPI_BUF_BYTES;
     }
     // dynamic shared memory to request (with slack for aligning the base)
     static __host__ __device__ constexpr int smem_bytes(int stages) { return bar_offset(stages) + BAR_AREA + SMEM_ALIGN; }
@@ -80,7 +90,7 @@ struct Layout {
 
 struct Params {
     int32_t M, N, K;
-    int32_t m_blocks, n_blocks, num_tiles, k_chunks;
+    int32_t m_blocks, n_blocks, num_tiles, k_chunks;  // num_tiles counts cluster tiles (CM row blocks each)
     int32_t stages;
     int32_t group_m;       // tile raster: group_m row-blocks swept together for L2 reuse
     uint32_t idesc;        // tcgen05 instruction descriptor
@@ -94,14 +104,18 @@ struct Params {
     int64_t skip_load;     // test hook: this global K-chunk index is never copied (-1: off)
 };
 
-// Linear tile index -> (row block, column block), grouped raster.
-__device__ __forceinline__ void tile_coords(int tile, const Params& p, int& mb, int& nb) {
+// Linear cluster-tile index -> (row block of this CTA, column block), with a
+// grouped raster over cluster row blocks (CM row blocks each): group_m of
+// them are swept together for L2 reuse.
+template <int CM>
+__device__ __forceinline__ void tile_coords(int tile, const Params& p, uint32_t rank, int& mb, int& nb) {
+    const int mc_blocks = (p.m_blocks + CM - 1) / CM;
     const int per_group = p.group_m * p.n_blocks;
     const int g = tile / per_group;
     const int first_m = g * p.group_m;
-    const int gsize = min(p.m_blocks - first_m, p.group_m);
+    const int gsize = min(mc_blocks - first_m, p.group_m);
     const int r = tile - g * per_group;
-    mb = first_m + r % gsize;
+    mb = (first_m + r % gsize) * CM + static_cast<int>(rank);
     nb = r / gsize;
 }
 
@@ -146,6 +160,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2_relu(float lo, float hi) {
+    if constexpr (OUT == SG_F16) {
+        return cvt_relu_f16x2(lo, hi);
+    } else {
+        return cvt_relu_bf16x2(lo, hi);
+    }
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -161,11 +184,40 @@ __device__ __forceinline__ void store_one(void* C, int64_t idx, float v) {
     }
 }
 
-template <int BN, int OUT>
+// + bias[col] for the COLS columns starting at col0 (zero past N).
+template <int COLS>
+__device__ __forceinline__ void add_bias(float (&v)[COLS], const float* __restrict__ bias, int col0, int N) {
+    if (col0 + COLS <= N && (reinterpret_cast<uintptr_t>(bias + col0) & 15) == 0) {
+        const float4* b4 = reinterpret_cast<const float4*>(bias + col0);
+#pragma unroll
+        for (int i = 0; i < COLS / 4; ++i) {
+            const float4 b = __ldg(b4 + i);
+            v[4 * i + 0] += b.x;
+            v[4 * i + 1] += b.y;
+            v[4 * i + 2] += b.z;
+            v[4 * i + 3] += b.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < COLS; ++i) {
+            const int col = col0 + i;
+            v[i] += (col < N) ? __ldg(bias + col) : 0.0f;
+        }
+    }
+}
+
+template <int BN, int OUT, int CM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const Params p) {
     using L = Layout<BN>;
+    static_assert(CM == 1 || CM == 2, "cluster size 1 or 2");
+    static_assert((BN / 64) % CM == 0, "each CTA of a cluster copies whole B boxes");
+    constexpr uint16_t CLUSTER_MASK = static_cast<uint16_t>((1u << CM) - 1u);
+    const uint32_t rank = (CM > 1) ? cluster_ctarank() : 0u;
+    const int cluster_id = static_cast<int>(blockIdx.x) / CM;
+    const int num_clusters = static_cast<int>(gridDim.x) / CM;
+    constexpr int ACC = L::ACC;
     constexpr int COLS = (OUT == SG_F32) ? 32 : 64;  // output columns per 128-byte staging row
     static_assert(BN % COLS == 0, "tile width must hold whole staging rows");
 
@@ -176,13 +228,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int stages = p.stages;
 
     const uint32_t bar0 = base + L::bar_offset(stages);
-    // barrier slots: full[0..7], empty[8..15], tmem_full[16..17], tmem_empty[18..19], drain[20]
+    // barrier slots: full[0..7], empty[8..15], tmem_full[16..19], tmem_empty[20..23], drain[24]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (SG_MAX_STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * SG_MAX_STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::bar_offset(stages) + 8 * (2 * SG_MAX_STAGES + 5));
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + MAX_ACC + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * SG_MAX_STAGES + 2 * MAX_ACC);
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(gbase + L::bar_offset(stages) + 8 * (2 * SG_MAX_STAGES + 2 * MAX_ACC + 1));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -191,9 +244,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CM);  // one MMA commit from each CTA of the cluster
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < ACC; ++b) {
             mbar_init(tfull_bar(b), 1);
             mbar_init(tempty_bar(b), EPI_WARPS);
         }
@@ -210,11 +263,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     __syncwarp();  // reconverge before the warp-collective (.sync.aligned) instructions below
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
+        tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // the peer's barriers must be initialised before any multicast reaches them
+    if constexpr (CM > 1) {
+        cluster_sync();
+    } else {
+        __syncthreads();
+    }
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -225,9 +283,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued = 0, last_parity = 0;  // per slot: ever filled, parity of its last fill
             int64_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 int mb, nb;
-                tile_coords(tile, p, mb, nb);
+                tile_coords<CM>(tile, p, rank, mb, nb);
                 for (int kc = 0; kc < p.k_chunks; ++kc, ++it) {
                     if (!wait_bounded(empty_bar(slot), phase ^ 1u, abort_flag, p.status, p.wait_limit_ns,
                                       SITE_PRODUCER_EMPTY)) {
@@ -239,9 +297,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_expect_tx(full_bar(slot), L::STAGE_BYTES);
                         tma_load_2d(sa, &tmA, full_bar(slot), kc * BK, mb * BM);
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(sa + A_STAGE_BYTES + j * B_CHUNK_BYTES, &tmB, full_bar(slot), nb * BN + j * 64,
-                                        kc * BK);
+                        for (int j = 0; j < BN / 64; ++j) {
+                            const uint32_t dst = sa + A_STAGE_BYTES + j * B_CHUNK_BYTES;
+                            if constexpr (CM == 1) {
+                                tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK);
+                            } else if (j % CM == static_cast<int>(rank)) {
+                                tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK,
+                                                      CLUSTER_MASK);
+                            }
+                        }
                         issued |= 1u << slot;
                         last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
                     }
@@ -261,10 +325,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------ MMA issuer
         if (lane == 0 && p.k_chunks > 0) {
             uint32_t slot = 0, phase = 0;
+            uint32_t ab = 0, aph = 0;  // accumulator index and its phase
             bool ok = true;
-            int lt = 0;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++lt) {
-                const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 if (!wait_bounded(tempty_bar(ab), aph ^ 1u, abort_flag, p.status, p.wait_limit_ns,
                                   SITE_MMA_TMEM_EMPTY)) {
                     ok = false;
@@ -283,13 +346,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // groups 1024 B apart, 64-column blocks one TMA box apart.
                     const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
                     const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE_BYTES, B_CHUNK_BYTES, 1024);
+                    // K steps that lie wholly past K would only add products of
+                    // zero-filled elements: skip them
+                    const int ksteps = min(BK / UMMA_K, (p.K - kc * BK + UMMA_K - 1) / UMMA_K);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
-                        umma_f16(d_tmem, a_desc + ((k * UMMA_K * 2) >> 4), b_desc + ((k * UMMA_K * 128) >> 4),
-                                 p.idesc, (kc | k) != 0 ? 1u : 0u);
+                        if (k < ksteps)
+                            umma_f16(d_tmem, a_desc + ((k * UMMA_K * 2) >> 4), b_desc + ((k * UMMA_K * 128) >> 4),
+                                     p.idesc, (kc | k) != 0 ? 1u : 0u);
                     }
-                    umma_commit(empty_bar(slot));
+                    if constexpr (CM == 1) {
+                        umma_commit(empty_bar(slot));
+                    } else {
+                        umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slot in both CTAs
+                    }
                     if (++slot == static_cast<uint32_t>(stages)) {
                         slot = 0;
                         phase ^= 1u;
@@ -297,6 +368,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 umma_commit(tfull_bar(ab));
+                if (++ab == static_cast<uint32_t>(ACC)) {
+                    ab = 0;
+                    aph ^= 1u;
+                }
             }
             // every MMA of this CTA has completed before tensor memory is released
             umma_commit(drain_bar);
@@ -304,14 +379,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ------------------------------------------------ epilogue
-        const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
-        const uint32_t stage0 = base + L::epi_offset(stages) + (warp - 2) * EPI_BUFS * EPI_BUF_BYTES;
-        uint32_t buf_i = 0;
-        int lt = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++lt) {
-            const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
+        const int e = warp - 2;                   // 0 .. EPI_WARPS-1
+        const int q = warp & 3;                   // the tensor-memory lane quarter this warp may read
+        constexpr int SPLIT = EPI_WARPS / 4;      // warps sharing a quarter
+        const int part = e / 4;                   // which of them: takes column chunks part, part+SPLIT, ...
+        const uint32_t buf = base + L::epi_offset(stages) + e * EPI_BUF_BYTES;
+        uint32_t ab = 0, aph = 0;
+        for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
             int mb, nb;
-            tile_coords(tile, p, mb, nb);
+            tile_coords<CM>(tile, p, rank, mb, nb);
             if (p.k_chunks > 0) {
                 const bool w = wait_bounded(tfull_bar(ab), aph, abort_flag, p.status, p.wait_limit_ns,
                                             SITE_EPI_TMEM_FULL);
@@ -322,7 +398,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row = row0 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += COLS) {
+            for (int c = part * COLS; c < BN; c += SPLIT * COLS) {
                 const int col0 = nb * BN + c;
                 float v[COLS];
                 if (p.k_chunks > 0) {
@@ -344,21 +420,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < COLS; ++i) v[i] = 0.0f;
                 }
-                if (p.epi == SG_EPI_BIAS_RELU) {
+                if (p.epi == SG_EPI_BIAS_RELU) add_bias<COLS>(v, p.bias, col0, p.N);
+                const bool relu = p.epi != SG_EPI_NONE;
+                if (OUT == SG_F32 || !p.tma_store) {
+                    if (relu) {
 #pragma unroll
-                    for (int i = 0; i < COLS; ++i) {
-                        const int col = col0 + i;
-                        v[i] += (col < p.N) ? __ldg(p.bias + col) : 0.0f;
+                        for (int i = 0; i < COLS; ++i) v[i] = (v[i] <= 0.0f) ? 0.0f : v[i];
                     }
-                }
-                if (p.epi != SG_EPI_NONE) {
-#pragma unroll
-                    for (int i = 0; i < COLS; ++i) v[i] = (v[i] <= 0.0f) ? 0.0f : v[i];
                 }
                 if (p.tma_store) {
                     if (row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
-                        const uint32_t buf = stage0 + (buf_i & 1u) * EPI_BUF_BYTES;
-                        if (lane == 0) bulk_wait_group_read<1>();  // the store that used this buffer has read it
+                        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
                         __syncwarp();
                         const uint32_t rowaddr = buf + lane * 128;
 #pragma unroll
@@ -369,6 +441,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 w1 = __float_as_uint(v[4 * j + 1]);
                                 w2 = __float_as_uint(v[4 * j + 2]);
                                 w3 = __float_as_uint(v[4 * j + 3]);
+                            } else if (relu) {
+                                w0 = pack2_relu<OUT>(v[8 * j + 0], v[8 * j + 1]);
+                                w1 = pack2_relu<OUT>(v[8 * j + 2], v[8 * j + 3]);
+                                w2 = pack2_relu<OUT>(v[8 * j + 4], v[8 * j + 5]);
+                                w3 = pack2_relu<OUT>(v[8 * j + 6], v[8 * j + 7]);
                             } else {
                                 w0 = pack2<OUT>(v[8 * j + 0], v[8 * j + 1]);
                                 w1 = pack2<OUT>(v[8 * j + 2], v[8 * j + 3]);
@@ -384,7 +461,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tma_store_2d(&tmC, buf, col0, row0);
                             bulk_commit_group();
                         }
-                        ++buf_i;
                     }
                 } else if (row < p.M) {
 #pragma unroll
@@ -400,6 +476,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(ab));
             }
+            if (++ab == static_cast<uint32_t>(ACC)) {
+                ab = 0;
+                aph ^= 1u;
+            }
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
@@ -407,10 +487,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     __syncwarp();  // lanes that skipped a lane-0 role wait for it here
     tc_fence_before();
-    __syncthreads();
+    // no CTA leaves while its peer may still multicast into it or arrive on it
+    if constexpr (CM > 1) {
+        cluster_sync();
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, L::TMEM_COLS);
+        tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

@@ -15,6 +15,17 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of every CTA in the cluster; orders memory at cluster scope.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -92,6 +103,18 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// The same load delivered to the same shared-memory offset of every CTA of
+// the cluster in `mask`, completing bytes on the barrier at the same offset
+// in each of them.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, uint32_t bar, int32_t x,
+                                                      int32_t y, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
 // 2-D tiled store shared -> global.  Elements outside the tensor map's
 // extents are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
@@ -166,6 +189,15 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// As umma_commit, arriving on the barrier at the same offset in every CTA of
+// the cluster in `mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"(mask)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
 // lane (taddr.lane + t), columns taddr.col .. taddr.col + 31.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -194,6 +226,24 @@ __device__ __forceinline__ void tmem_wait_ld_dep(uint32_t (&r)[32]) {
           "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
         :
         : "memory");
+}
+
+// ------------------------------------------------------------ conversions
+
+// Two fp32 values -> packed fp16x2 / bf16x2 (lo in the low half, i.e. at the
+// lower address), round to nearest even, with ReLU applied by the conversion
+// (negative -> +0, NaN stays NaN).  max(x, 0) commutes with a monotonic
+// rounding that maps 0 to 0, so this equals rounding the ReLU'd value.
+__device__ __forceinline__ uint32_t cvt_relu_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.relu.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t cvt_relu_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // --------------------------------------------------------------- descriptors

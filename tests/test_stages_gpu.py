@@ -72,3 +72,76 @@ def test_stage_count_rejected_when_too_deep():
     with pytest.raises(sg.SgError) as e:
         sg.stage_gemm(A, B, out_dtype=torch.bfloat16, stages=p["max_stages"] + 1)
     assert e.value.code == -3
+
+
+def test_tile_widths_bit_identical():
+    """gizml:tile, "tune": every configuration computes the same result.  The
+    128-, 192- and 256-column tiles sum the same products in the same K
+    order, so their outputs must agree bit for bit."""
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = sg.load_library()
+    M, N, K = 1100, 1152, 300
+    a, b = seeded_case(M, N, K, "f16", seed=23, lda=304)
+    outs = {}
+    try:
+        for bn in (128, 192, 256):
+            assert lib.sg_test_set_tile_n(bn) == 0
+            assert _plan(M, N, K, "f16", "f16")["block_n"] == bn
+            outs[bn] = run_gpu(a, b, M, N, K, "f16", "f16", "relu")
+    finally:
+        lib.sg_test_set_tile_n(0)
+    assert np.array_equal(outs[128], outs[192]) and np.array_equal(outs[128], outs[256])
+    ref, _, S = oracle.gemm(a, b, "f16", "f16", "relu", K=K)
+    compare(outs[128], ref, S, "f16", "tile widths")
+
+
+def test_stage_counts_bit_identical_bn192():
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = sg.load_library()
+    M, N, K = 700, 576, 200
+    a, b = seeded_case(M, N, K, "bf16", seed=24, lda=208)
+    try:
+        assert lib.sg_test_set_tile_n(192) == 0
+        p = _plan(M, N, K, "bf16", "f32")
+        assert p["block_n"] == 192 and p["max_stages"] >= 3
+        outs = [run_gpu(a, b, M, N, K, "bf16", "f32", stages=s) for s in range(1, p["max_stages"] + 1)]
+    finally:
+        lib.sg_test_set_tile_n(0)
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    ref, _, S = oracle.gemm(a, b, "bf16", "f32", K=K)
+    compare(outs[0], ref, S, "f32", "bn192")
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_cluster_multicast_bit_identical(bn):
+    """Sharing each B tile between two CTAs by TMA multicast changes only who
+    copies what: C must be bit-identical to the single-CTA path, at every
+    stage count, including an odd number of row blocks (the last cluster's
+    second CTA owns a tile wholly below M)."""
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = sg.load_library()
+    M, N, K = 1000, 1024, 640          # 8 row blocks (ragged) ...
+    M2 = 1130                          # ... and 9 (odd)
+    outs = {}
+    try:
+        assert lib.sg_test_set_tile_n(bn) == 0
+        for m in (M, M2):
+            a, b = seeded_case(m, N, K, "bf16", seed=25 + m, dist=("uniform", -1.0, 1.0))
+            for cm in (1, 2):
+                assert lib.sg_test_set_cluster(cm) == 0
+                p = _plan(m, N, K, "bf16", "bf16")
+                assert p["cluster_m"] == cm and p["block_n"] == bn
+                for st in (1, 2, p["max_stages"]):
+                    outs[(m, cm, st)] = run_gpu(a, b, m, N, K, "bf16", "bf16", stages=st)
+            ref_rows = np.arange(m)
+            rng = np.random.default_rng(m)
+            rows = np.concatenate([rng.integers(0, m, 2000), np.full(N, m - 1)])
+            cols = np.concatenate([rng.integers(0, N, 2000), np.arange(N)])
+            ref, _, S = oracle.gemm_at(a, b, rows, cols, "bf16", "bf16")
+            compare(outs[(m, 2, 1)][rows, cols], ref, S, "bf16", f"cluster m={m}")
+    finally:
+        lib.sg_test_set_cluster(0)
+        lib.sg_test_set_tile_n(0)
+    for (m, cm, st), o in outs.items():
+        assert np.array_equal(o, outs[(m, 1, 1)]), (m, cm, st)
