@@ -133,8 +133,12 @@ typedef struct {
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t tmem_columns;  /* tensor-memory columns allocated per CTA */
     int32_t tma_store;     /* 1: C written by TMA stores, 0: masked stores */
-    int32_t cluster_m;     /* CTAs per cluster sharing each B tile by multicast (1 or 2) */
-    int32_t reserved[4];
+    int32_t cluster_m;     /* CTAs per cluster (1 or 2) */
+    int32_t pair_mma;      /* 1: the cluster's two CTAs compute one 256-row tile
+                              with the paired MMA; 0: one CTA per 128-row tile
+                              (with cluster_m 2: the pair shares each B tile by
+                              multicast) */
+    int32_t reserved[3];
 } sg_plan_info;
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,

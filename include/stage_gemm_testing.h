@@ -38,14 +38,17 @@ int sg_test_set_skip_load(int64_t it);
 int sg_test_set_tile_n(int bn);
 
 /*
- * Forces the cluster size of later sg_gemm / sg_plan calls: 1 (every CTA
- * copies its whole B tile) or 2 (two CTAs with vertically adjacent tiles
- * share each B tile through TMA multicast; only for tile widths of 128 or
- * 256); 0 restores the planner's choice.  Both issue the same MMAs in the
- * same order, so C must be bit-identical.  Returns 0, or SG_ERR_ARG.  The
- * environment variable STAGE_GEMM_CLUSTER sets the initial value at load.
+ * Forces the kernel mode of later sg_gemm / sg_plan calls: 1 (one CTA per
+ * 128-row tile, copying its whole B tile), 2 (two CTAs with vertically
+ * adjacent tiles share each B tile through TMA multicast) or 3 (the two CTAs
+ * of a cluster compute one 256-row tile with the paired MMA, each staging
+ * half of B); modes 2 and 3 need a tile width of 128 or 256.  0 restores the
+ * planner's choice.  Every mode sums the same products in the same K order
+ * for each output element, so C must be bit-identical.  Returns 0, or
+ * SG_ERR_ARG.  The environment variable STAGE_GEMM_CLUSTER sets the initial
+ * value at load.
  */
-int sg_test_set_cluster(int cm);
+int sg_test_set_cluster(int mode);
 
 #ifdef __cplusplus
 }

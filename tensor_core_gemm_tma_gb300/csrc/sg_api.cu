@@ -20,7 +20,14 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kGroupM = 8;  // row blocks swept together by the tile raster
+// Cluster row blocks swept together by the tile raster (L2 reuse of the B
+// tiles they share); STAGE_GEMM_GROUP_M overrides it at load (tuning only:
+// the order of tiles never changes a result).
+const int kGroupM = [] {
+    const char* e = std::getenv("STAGE_GEMM_GROUP_M");
+    const int x = e ? std::atoi(e) : 0;
+    return (x >= 1 && x <= 64) ? x : 8;
+}();
 
 struct DevState {
     bool ready = false;
@@ -29,8 +36,8 @@ struct DevState {
     int smem_per_sm = 0;
     int major = 0, minor = 0;
     int* status = nullptr;  // device status word (4 bytes, library-owned)
-    bool attr_done[3][3][2] = {};  // [tile-width variant][output type][cluster variant]
-    int max_clusters[3][3][2] = {};  // co-resident clusters of each instantiation (0: not queried)
+    bool attr_done[3][3][3] = {};    // [tile-width variant][output type][mode - 1]
+    int max_clusters[3][3][3] = {};  // co-resident clusters of each instantiation (0: not queried)
 };
 
 std::mutex g_mu;
@@ -136,7 +143,8 @@ int device_state(DevState** out) {
 
 struct Plan {
     int bn = 128;
-    int cm = 1;  // CTAs per cluster along M (B tile multicast when 2)
+    int mode = 1;  // 1: single CTA, 2: CTA pairs sharing B by multicast, 3: paired MMA
+    int cm = 1;    // CTAs per cluster along M
     int stages = 0, max_stages = 0;
     int64_t m_blocks = 0, n_blocks = 0, tiles = 0, k_chunks = 0;
     int grid = 0;
@@ -145,14 +153,18 @@ struct Plan {
     int tma_store = 0;
 };
 
-template <int BN>
-int layout_smem(int stages) { return sg::Layout<BN>::smem_bytes(stages); }
-
-int smem_for(int bn, int stages) {
+int smem_for(int bn, int stages, int mode) {
+    if (mode == 3) {  // each CTA stages half of B
+        switch (bn) {
+            case 128: return sg::Layout<128, 64>::smem_bytes(stages);
+            case 256: return sg::Layout<256, 128>::smem_bytes(stages);
+            default: return -1;
+        }
+    }
     switch (bn) {
-        case 128: return layout_smem<128>(stages);
-        case 192: return layout_smem<192>(stages);
-        case 256: return layout_smem<256>(stages);
+        case 128: return sg::Layout<128>::smem_bytes(stages);
+        case 192: return sg::Layout<192>::smem_bytes(stages);
+        case 256: return sg::Layout<256>::smem_bytes(stages);
         default: return -1;
     }
 }
@@ -168,12 +180,13 @@ std::atomic<int> g_force_bn{[] {
 }()};
 int forced_bn() { return g_force_bn.load(); }
 
-// Cluster size forced by sg_test_set_cluster or, at load, the environment
-// variable STAGE_GEMM_CLUSTER (1 or 2; 0: the planner's choice).
-std::atomic<int> g_force_cm{[] {
+// Kernel mode forced by sg_test_set_cluster or, at load, the environment
+// variable STAGE_GEMM_CLUSTER (1: single CTA, 2: CTA pairs sharing B by
+// multicast, 3: paired MMA; 0: the planner's choice).
+std::atomic<int> g_force_mode{[] {
     const char* e = std::getenv("STAGE_GEMM_CLUSTER");
     const int x = e ? std::atoi(e) : 0;
-    return (x == 1 || x == 2) ? x : 0;
+    return (x >= 1 && x <= 3) ? x : 0;
 }()};
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype, const void* C, int64_t ldc,
@@ -198,24 +211,27 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
     if (forced_bn()) bn = forced_bn();
     pl->bn = bn;
     pl->n_blocks = cdiv(N, bn);
-    // Pairs of CTAs share each B tile (multicast) when the problem is large
-    // and the K loop long enough for operand traffic to matter.
-    int cm = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pl->m_blocks * pl->n_blocks >= st.sm_count &&
-              (bn / 64) % 2 == 0)
-                 ? 2
-                 : 1;
-    if (const int f = g_force_cm.load(); f == 1 || (f == 2 && (bn / 64) % 2 == 0)) cm = f;
-    pl->cm = cm;
+    // Pairs of CTAs compute 256-row tiles with the paired MMA when the
+    // problem is large and the K loop long enough for operand traffic to
+    // matter: each SM then stages only its half of B.
+    const bool pairable = (bn / 64) % 2 == 0;
+    int mode = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pl->m_blocks * pl->n_blocks >= st.sm_count && pairable)
+                   ? 3
+                   : 1;
+    if (const int f = g_force_mode.load(); f == 1 || (f >= 2 && pairable)) mode = f;
+    pl->mode = mode;
+    pl->cm = mode == 1 ? 1 : 2;
+    const int cm = pl->cm;
     pl->tiles = cdiv(pl->m_blocks, cm) * pl->n_blocks;  // cluster tiles
     int maxs = 0;
     for (int s = 1; s <= SG_MAX_STAGES; ++s)
-        if (smem_for(bn, s) <= st.smem_optin) maxs = s;
+        if (smem_for(bn, s, mode) <= st.smem_optin) maxs = s;
     pl->max_stages = maxs;
     if (maxs == 0) return SG_ERR_STAGES;
     if (stages == 0) stages = maxs;
     if (stages > maxs) return SG_ERR_STAGES;
     pl->stages = stages;
-    pl->smem = smem_for(bn, stages);
+    pl->smem = smem_for(bn, stages, mode);
     pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for
     // it; keep one persistent CTA per SM by asking for more than half of the
@@ -251,10 +267,11 @@ int encode_2d(CUtensorMap* tm, int dt, const void* ptr, int64_t inner, int64_t o
     return r == CUDA_SUCCESS ? SG_OK : SG_ERR_CUDA;
 }
 
-template <int BN, int OUT, int CM>
+template <int BN, int OUT, int MODE>
 int launch_t(DevState& st, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
              const sg::Params& prm, cudaStream_t stream) {
-    auto kern = sg::sg_gemm_kernel<BN, OUT, CM>;
+    constexpr int CM = MODE == 1 ? 1 : 2;
+    auto kern = sg::sg_gemm_kernel<BN, OUT, MODE>;
     const int bi = BN == 128 ? 0 : BN == 192 ? 1 : 2;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -270,14 +287,14 @@ int launch_t(DevState& st, const Plan& pl, const CUtensorMap& ta, const CUtensor
     int grid = pl.grid;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!st.attr_done[bi][OUT][CM - 1]) {
+        if (!st.attr_done[bi][OUT][MODE - 1]) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, st.smem_optin) !=
                 cudaSuccess)
                 return SG_ERR_CUDA;
-            st.attr_done[bi][OUT][CM - 1] = true;
+            st.attr_done[bi][OUT][MODE - 1] = true;
         }
         if (CM > 1) {
-            int& mc = st.max_clusters[bi][OUT][CM - 1];
+            int& mc = st.max_clusters[bi][OUT][MODE - 1];
             if (mc == 0) {
                 cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
                 int n = 0;
@@ -296,19 +313,23 @@ int launch_t(DevState& st, const Plan& pl, const CUtensorMap& ta, const CUtensor
     return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
 }
 
-template <int BN, int CM>
+template <int BN, int MODE>
 int launch_bn(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
               const CUtensorMap& tc, const sg::Params& prm, cudaStream_t stream) {
     switch (out_dtype) {
-        case SG_F32: return launch_t<BN, SG_F32, CM>(st, pl, ta, tb, tc, prm, stream);
-        case SG_F16: return launch_t<BN, SG_F16, CM>(st, pl, ta, tb, tc, prm, stream);
-        default: return launch_t<BN, SG_BF16, CM>(st, pl, ta, tb, tc, prm, stream);
+        case SG_F32: return launch_t<BN, SG_F32, MODE>(st, pl, ta, tb, tc, prm, stream);
+        case SG_F16: return launch_t<BN, SG_F16, MODE>(st, pl, ta, tb, tc, prm, stream);
+        default: return launch_t<BN, SG_BF16, MODE>(st, pl, ta, tb, tc, prm, stream);
     }
 }
 
 int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
                 const CUtensorMap& tc, const sg::Params& prm, cudaStream_t stream) {
-    if (pl.cm == 2) {
+    if (pl.mode == 3) {
+        if (pl.bn == 256) return launch_bn<256, 3>(st, out_dtype, pl, ta, tb, tc, prm, stream);
+        return launch_bn<128, 3>(st, out_dtype, pl, ta, tb, tc, prm, stream);
+    }
+    if (pl.mode == 2) {
         if (pl.bn == 256) return launch_bn<256, 2>(st, out_dtype, pl, ta, tb, tc, prm, stream);
         return launch_bn<128, 2>(st, out_dtype, pl, ta, tb, tc, prm, stream);
     }
@@ -357,7 +378,7 @@ int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
     prm.group_m = kGroupM;
-    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, sg::BM, pl.bn, true);
+    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, pl.mode == 3 ? 2 * sg::BM : sg::BM, pl.bn, true);
     prm.epi = epilogue;
     prm.tma_store = pl.tma_store;
     prm.bias = bias;
@@ -395,6 +416,7 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
     info->tmem_columns = pl.tmem_cols;
     info->tma_store = pl.tma_store;
     info->cluster_m = pl.cm;
+    info->pair_mma = pl.mode == 3 ? 1 : 0;
     return SG_OK;
 }
 
@@ -447,9 +469,9 @@ int sg_test_set_tile_n(int bn) {
     return SG_OK;
 }
 
-int sg_test_set_cluster(int cm) {
-    if (cm < 0 || cm > 2) return SG_ERR_ARG;
-    g_force_cm.store(cm);
+int sg_test_set_cluster(int mode) {
+    if (mode < 0 || mode > 3) return SG_ERR_ARG;
+    g_force_mode.store(mode);
     return SG_OK;
 }
 
@@ -537,7 +559,7 @@ int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
     prm.group_m = kGroupM;
-    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, sg::BM, pl.bn, true);
+    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, pl.mode == 3 ? 2 * sg::BM : sg::BM, pl.bn, true);
     prm.epi = epilogue;
     prm.tma_store = pl.tma_store;
     prm.bias = bias;

@@ -24,11 +24,22 @@
 //               TMA store that does not write elements outside M x N
 //               (gizml:tile, "Out.put").
 //
-// Clusters (CM = 2): the two CTAs of a cluster own vertically adjacent tiles
-// with the same column block, so they need the same B tile.  Each copies half
-// of its 64-column boxes and multicasts them to both CTAs' rings, halving the
-// B traffic from L2; a ring slot is free only when both CTAs' MMAs have read
-// it (the empty barrier counts one commit from each CTA).
+// Three modes (MODE):
+//   1  one CTA per 128 x BN tile.
+//   2  clusters of two CTAs with vertically adjacent 128 x BN tiles and the
+//      same column block: each CTA copies half of the B tile's 64-column
+//      boxes and multicasts them into both CTAs' rings, halving the B
+//      traffic from L2; a ring slot is free only when both CTAs' MMAs have
+//      read it (the empty barrier counts one commit from each CTA).
+//   3  paired MMA (tcgen05 cta_group::2): the two CTAs of a cluster compute
+//      one 256 x BN tile.  Each CTA stages its own 128 rows of A and its own
+//      BN/2 columns of B (so a stage is 32 KiB instead of 48 KiB for
+//      BN = 256 and the ring is 6 deep); one thread of the even CTA issues
+//      the MMAs, whose accumulator rows live in each CTA's own tensor
+//      memory.  Both CTAs' copies complete on the even CTA's full barrier;
+//      its commits free the ring slots and hand accumulators to the
+//      epilogues of both CTAs; both epilogues release accumulators on the
+//      even CTA's barrier.
 //
 // The ring generalises the two-slot pipeline of Tolk.Stage (copy chunk k+1
 // into slot (k+1) mod 2 while computing on slot k mod 2) and the `stages`
@@ -74,10 +85,13 @@ constexpr int BAR_AREA = 256;
 constexpr int STATUS_TIMEOUT = 0x5400;
 constexpr int SITE_PRODUCER_EMPTY = 1, SITE_MMA_TMEM_EMPTY = 2, SITE_MMA_FULL = 3, SITE_EPI_TMEM_FULL = 4;
 
-template <int BN>
+// BN: accumulator columns per tile; BL: B columns this CTA stages per K chunk
+// (BN, or BN / 2 for the paired MMA).
+template <int BN, int BL = BN>
 struct Layout {
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
-    static constexpr int B_STAGE_BYTES = BK * BN * 2;
+    static_assert(BL % 64 == 0 && BL <= BN, "B is staged in whole 64-column boxes");
+    static constexpr int B_STAGE_BYTES = BK * BL * 2;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int ACC = (TMEM_COLS / BN) < MAX_ACC ? (TMEM_COLS / BN) : MAX_ACC;
     static __host__ __device__ constexpr int epi_offset(int stages) { return stages * STAGE_BYTES; }
@@ -206,13 +220,17 @@ __device__ __forceinline__ void add_bias(float (&v)[COLS], const float* __restri
     }
 }
 
-template <int BN, int OUT, int CM>
+template <int BN, int OUT, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const Params p) {
-    using L = Layout<BN>;
-    static_assert(CM == 1 || CM == 2, "cluster size 1 or 2");
-    static_assert((BN / 64) % CM == 0, "each CTA of a cluster copies whole B boxes");
+    static_assert(MODE >= 1 && MODE <= 3, "mode 1, 2 or 3");
+    constexpr int CM = (MODE == 1) ? 1 : 2;    // CTAs per cluster
+    constexpr bool PAIR = (MODE == 3);         // paired MMA (cta_group::2)
+    constexpr int CG = PAIR ? 2 : 1;           // cta_group of every tcgen05 instruction
+    constexpr int BL = PAIR ? BN / 2 : BN;     // B columns staged by this CTA
+    using L = Layout<BN, BL>;
+    static_assert((BL / 64) % (MODE == 2 ? 2 : 1) == 0, "each CTA of a cluster copies whole B boxes");
     constexpr uint16_t CLUSTER_MASK = static_cast<uint16_t>((1u << CM) - 1u);
     const uint32_t rank = (CM > 1) ? cluster_ctarank() : 0u;
     const int cluster_id = static_cast<int>(blockIdx.x) / CM;
@@ -244,11 +262,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CM);  // one MMA commit from each CTA of the cluster
+            mbar_init(empty_bar(s), MODE == 2 ? 2 : 1);  // mode 2: one MMA commit from each CTA
         }
         for (int b = 0; b < ACC; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), EPI_WARPS);
+            mbar_init(tempty_bar(b), PAIR ? 2 * EPI_WARPS : EPI_WARPS);  // paired: both CTAs' epilogues
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -263,8 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     __syncwarp();  // reconverge before the warp-collective (.sync.aligned) instructions below
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_addr(tmem_slot), TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     // the peer's barriers must be initialised before any multicast reaches them
@@ -294,16 +312,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     if (it != p.skip_load) {
                         const uint32_t sa = base + slot * L::STAGE_BYTES;
-                        mbar_arrive_expect_tx(full_bar(slot), L::STAGE_BYTES);
-                        tma_load_2d(sa, &tmA, full_bar(slot), kc * BK, mb * BM);
+                        if constexpr (PAIR) {
+                            // both CTAs' copies complete on the even CTA's barrier
+                            const uint32_t fb = mapa_shared(full_bar(slot), 0);
+                            if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), 2 * L::STAGE_BYTES);
+                            tma_load_2d_pair(sa, &tmA, fb, kc * BK, mb * BM);
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j) {
-                            const uint32_t dst = sa + A_STAGE_BYTES + j * B_CHUNK_BYTES;
-                            if constexpr (CM == 1) {
-                                tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK);
-                            } else if (j % CM == static_cast<int>(rank)) {
-                                tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK,
-                                                      CLUSTER_MASK);
+                            for (int j = 0; j < BL / 64; ++j)
+                                tma_load_2d_pair(sa + A_STAGE_BYTES + j * B_CHUNK_BYTES, &tmB, fb,
+                                                 nb * BN + static_cast<int>(rank) * BL + j * 64, kc * BK);
+                        } else {
+                            mbar_arrive_expect_tx(full_bar(slot), L::STAGE_BYTES);
+                            tma_load_2d(sa, &tmA, full_bar(slot), kc * BK, mb * BM);
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j) {
+                                const uint32_t dst = sa + A_STAGE_BYTES + j * B_CHUNK_BYTES;
+                                if constexpr (MODE == 1) {
+                                    tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK);
+                                } else if (j % 2 == static_cast<int>(rank)) {
+                                    tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK,
+                                                          CLUSTER_MASK);
+                                }
                             }
                         }
                         issued |= 1u << slot;
@@ -315,15 +344,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (!ok) {
-                // the CTA is leaving early: let this warp's copies land first
+            if (!ok && (!PAIR || rank == 0)) {
+                // the CTA is leaving early: let this warp's copies land first (paired: the
+                // even CTA's barriers also count the odd CTA's copies)
                 for (int s = 0; s < stages; ++s)
                     if ((issued >> s) & 1u) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0 && p.k_chunks > 0) {
+        if (lane == 0 && p.k_chunks > 0 && (!PAIR || rank == 0)) {
             uint32_t slot = 0, phase = 0;
             uint32_t ab = 0, aph = 0;  // accumulator index and its phase
             bool ok = true;
@@ -352,14 +382,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
-                        if (k < ksteps)
-                            umma_f16(d_tmem, a_desc + ((k * UMMA_K * 2) >> 4), b_desc + ((k * UMMA_K * 128) >> 4),
-                                     p.idesc, (kc | k) != 0 ? 1u : 0u);
+                        if (k < ksteps) {
+                            const uint64_t ad = a_desc + ((k * UMMA_K * 2) >> 4);
+                            const uint64_t bd = b_desc + ((k * UMMA_K * 128) >> 4);
+                            const uint32_t acc = (kc | k) != 0 ? 1u : 0u;
+                            if constexpr (PAIR) {
+                                umma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
+                            } else {
+                                umma_f16(d_tmem, ad, bd, p.idesc, acc);
+                            }
+                        }
                     }
-                    if constexpr (CM == 1) {
+                    if constexpr (MODE == 1) {
                         umma_commit(empty_bar(slot));
-                    } else {
+                    } else if constexpr (MODE == 2) {
                         umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slot in both CTAs
+                    } else {
+                        umma_commit_pair_multicast(empty_bar(slot), CLUSTER_MASK);
                     }
                     if (++slot == static_cast<uint32_t>(stages)) {
                         slot = 0;
@@ -367,14 +406,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(ab));
+                if constexpr (PAIR) {
+                    umma_commit_pair_multicast(tfull_bar(ab), CLUSTER_MASK);  // both CTAs' epilogues
+                } else {
+                    umma_commit(tfull_bar(ab));
+                }
                 if (++ab == static_cast<uint32_t>(ACC)) {
                     ab = 0;
                     aph ^= 1u;
                 }
             }
             // every MMA of this CTA has completed before tensor memory is released
-            umma_commit(drain_bar);
+            if constexpr (PAIR) {
+                umma_commit_pair(drain_bar);
+            } else {
+                umma_commit(drain_bar);
+            }
             wait_drain(drain_bar, 0, p.wait_limit_ns);
         }
     } else {
@@ -474,7 +521,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (p.k_chunks > 0) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(ab));
+                if (lane == 0) {
+                    if constexpr (PAIR) {
+                        mbar_arrive_cluster(mapa_shared(tempty_bar(ab), 0));  // the even CTA's MMA waits on it
+                    } else {
+                        mbar_arrive(tempty_bar(ab));
+                    }
+                }
             }
             if (++ab == static_cast<uint32_t>(ACC)) {
                 ab = 0;
@@ -495,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, TMEM_COLS);
     }
 }
 

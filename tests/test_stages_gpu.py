@@ -113,35 +113,54 @@ def test_stage_counts_bit_identical_bn192():
     compare(outs[0], ref, S, "f32", "bn192")
 
 
-@pytest.mark.parametrize("bn", [128, 256])
-def test_cluster_multicast_bit_identical(bn):
-    """Sharing each B tile between two CTAs by TMA multicast changes only who
-    copies what: C must be bit-identical to the single-CTA path, at every
-    stage count, including an odd number of row blocks (the last cluster's
-    second CTA owns a tile wholly below M)."""
+def test_paired_mma_small():
+    """The paired MMA (two CTAs, one 256-row tile) on a small case: every
+    row block pairing, a ragged K tail and an odd number of row blocks."""
     import tensor_core_gemm_tma_gb300 as sg
     lib = sg.load_library()
-    M, N, K = 1000, 1024, 640          # 8 row blocks (ragged) ...
-    M2 = 1130                          # ... and 9 (odd)
+    M, N, K = 300, 256, 200
+    a, b = seeded_case(M, N, K, "f16", seed=26, lda=208)
+    try:
+        assert lib.sg_test_set_cluster(3) == 0
+        p = _plan(M, N, K, "f16", "f32")
+        assert p["pair_mma"] == 1 and p["cluster_m"] == 2
+        got = run_gpu(a, b, M, N, K, "f16", "f32")
+    finally:
+        lib.sg_test_set_cluster(0)
+    ref, _, S = oracle.gemm(a, b, "f16", "f32", K=K)
+    compare(got, ref, S, "f32", "paired small")
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_cluster_modes_bit_identical(bn):
+    """Sharing each B tile between two CTAs by TMA multicast (mode 2) or
+    computing 256-row tiles with the paired MMA (mode 3) changes only who
+    copies and who issues: C must be bit-identical to the single-CTA path
+    (mode 1), at every stage count, including an odd number of row blocks
+    (the last cluster's second CTA owns rows wholly below M)."""
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = sg.load_library()
+    N, K = 1024, 640
     outs = {}
     try:
         assert lib.sg_test_set_tile_n(bn) == 0
-        for m in (M, M2):
+        for m in (1000, 1130):          # 8 row blocks (ragged), 9 (odd)
             a, b = seeded_case(m, N, K, "bf16", seed=25 + m, dist=("uniform", -1.0, 1.0))
-            for cm in (1, 2):
-                assert lib.sg_test_set_cluster(cm) == 0
+            for mode in (1, 2, 3):
+                assert lib.sg_test_set_cluster(mode) == 0
                 p = _plan(m, N, K, "bf16", "bf16")
-                assert p["cluster_m"] == cm and p["block_n"] == bn
-                for st in (1, 2, p["max_stages"]):
-                    outs[(m, cm, st)] = run_gpu(a, b, m, N, K, "bf16", "bf16", stages=st)
-            ref_rows = np.arange(m)
+                assert p["block_n"] == bn and p["cluster_m"] == (1 if mode == 1 else 2)
+                assert p["pair_mma"] == (1 if mode == 3 else 0)
+                for st in sorted({1, 2, p["max_stages"]}):
+                    outs[(m, mode, st)] = run_gpu(a, b, m, N, K, "bf16", "bf16", stages=st)
             rng = np.random.default_rng(m)
             rows = np.concatenate([rng.integers(0, m, 2000), np.full(N, m - 1)])
             cols = np.concatenate([rng.integers(0, N, 2000), np.arange(N)])
             ref, _, S = oracle.gemm_at(a, b, rows, cols, "bf16", "bf16")
-            compare(outs[(m, 2, 1)][rows, cols], ref, S, "bf16", f"cluster m={m}")
+            for mode in (1, 2, 3):
+                compare(outs[(m, mode, 1)][rows, cols], ref, S, "bf16", f"mode {mode} m={m}")
     finally:
         lib.sg_test_set_cluster(0)
         lib.sg_test_set_tile_n(0)
-    for (m, cm, st), o in outs.items():
-        assert np.array_equal(o, outs[(m, 1, 1)]), (m, cm, st)
+    for (m, mode, st), o in outs.items():
+        assert np.array_equal(o, outs[(m, 1, 1)]), (m, mode, st)
