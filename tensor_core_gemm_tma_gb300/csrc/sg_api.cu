@@ -151,20 +151,21 @@ struct Plan {
     int smem = 0;
     int tmem_cols = 0;
     int tma_store = 0;
+    int epi_bufs = 1;
 };
 
-int smem_for(int bn, int stages, int mode) {
+int smem_for(int bn, int stages, int mode, int bufs) {
     if (mode == 3) {  // each CTA stages half of B
         switch (bn) {
-            case 128: return sg::Layout<128, 64>::smem_bytes(stages);
-            case 256: return sg::Layout<256, 128>::smem_bytes(stages);
+            case 128: return sg::Layout<128, 64>::smem_bytes(stages, bufs);
+            case 256: return sg::Layout<256, 128>::smem_bytes(stages, bufs);
             default: return -1;
         }
     }
     switch (bn) {
-        case 128: return sg::Layout<128>::smem_bytes(stages);
-        case 192: return sg::Layout<192>::smem_bytes(stages);
-        case 256: return sg::Layout<256>::smem_bytes(stages);
+        case 128: return sg::Layout<128>::smem_bytes(stages, bufs);
+        case 192: return sg::Layout<192>::smem_bytes(stages, bufs);
+        case 256: return sg::Layout<256>::smem_bytes(stages, bufs);
         default: return -1;
     }
 }
@@ -223,15 +224,24 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
     pl->cm = mode == 1 ? 1 : 2;
     const int cm = pl->cm;
     pl->tiles = cdiv(pl->m_blocks, cm) * pl->n_blocks;  // cluster tiles
+    // One staging buffer per epilogue warp: measured on the skinny-K
+    // projection, a sixth ring stage is worth more than a second buffer.
+    // STAGE_GEMM_EPI_BUFS=2 (read at load) gives each warp two, for tuning.
+    static const int env_bufs = [] {
+        const char* e = std::getenv("STAGE_GEMM_EPI_BUFS");
+        return (e && std::atoi(e) == 2) ? 2 : 1;
+    }();
+    const int bufs = env_bufs;
+    pl->epi_bufs = bufs;
     int maxs = 0;
     for (int s = 1; s <= SG_MAX_STAGES; ++s)
-        if (smem_for(bn, s, mode) <= st.smem_optin) maxs = s;
+        if (smem_for(bn, s, mode, bufs) <= st.smem_optin) maxs = s;
     pl->max_stages = maxs;
     if (maxs == 0) return SG_ERR_STAGES;
     if (stages == 0) stages = maxs;
     if (stages > maxs) return SG_ERR_STAGES;
     pl->stages = stages;
-    pl->smem = smem_for(bn, stages, mode);
+    pl->smem = smem_for(bn, stages, mode, bufs);
     pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for
     // it; keep one persistent CTA per SM by asking for more than half of the
@@ -377,6 +387,7 @@ int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
     prm.num_tiles = static_cast<int32_t>(pl.tiles);
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
+    prm.epi_bufs = pl.epi_bufs;
     prm.group_m = kGroupM;
     prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, pl.mode == 3 ? 2 * sg::BM : sg::BM, pl.bn, true);
     prm.epi = epilogue;
@@ -558,6 +569,7 @@ int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     prm.num_tiles = static_cast<int32_t>(pl.tiles);
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
+    prm.epi_bufs = pl.epi_bufs;
     prm.group_m = kGroupM;
     prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, pl.mode == 3 ? 2 * sg::BM : sg::BM, pl.bn, true);
     prm.epi = epilogue;
