@@ -80,8 +80,7 @@ enum {
     SG_ERR_STAGES = -3,  /* stages < 0, > SG_MAX_STAGES, or does not fit in
                             shared memory for the chosen tile */
     SG_ERR_ALIAS = -4,   /* C overlaps A, B or bias */
-    SG_ERR_ALIGN = -5,   /* A or B base not 16-byte aligned, or lda/ldb times
-                            the element size not a multiple of 16 bytes */
+    SG_ERR_ALIGN = -5,   /* A or B not aligned to its 2-byte elements */
     SG_ERR_ARCH = -6,    /* the current device is not sm_103 */
     SG_ERR_CUDA = -7,    /* a CUDA runtime/driver call or the launch failed */
     SG_ERR_TIMEOUT = -8  /* a device-side wait gave up (reported by
@@ -107,10 +106,14 @@ enum {
  *               that fits, else 1..SG_MAX_STAGES.
  *   stream      cudaStream_t (as void*) the work is queued on.
  *
- * A and B must start on a 16-byte boundary and lda, ldb must be multiples of
- * 8 elements (TMA rule); otherwise SG_ERR_ALIGN.  C has no alignment rule:
- * an unaligned C uses a masked element-wise store epilogue instead of TMA
- * stores.
+ * Layouts: an operand whose base is 16-byte aligned and whose row pitch is
+ * a multiple of 16 bytes (lda, ldb multiples of 8 elements; any pitch for a
+ * single row) is staged by TMA.  Any other operand is staged by element
+ * loads of the producer warp into the same shared-memory layout (slower; the
+ * kernel then runs one CTA per tile); the results are bit-identical.  Only
+ * element alignment (2 bytes) is required, else SG_ERR_ALIGN.  C has no
+ * alignment rule: a C that is not 16-byte aligned or whose pitch is not a
+ * multiple of 16 bytes gets masked element stores instead of TMA stores.
  */
 int sg_gemm(int64_t M, int64_t N, int64_t K,
             const void* A, int64_t lda,
@@ -119,8 +122,9 @@ int sg_gemm(int64_t M, int64_t N, int64_t K,
             int in_dtype, int out_dtype, int epilogue,
             const float* bias, int stages, void* stream);
 
-/* The launch configuration sg_gemm would use (no GPU work is queued).
- * Needs a current CUDA device; returns the same codes as sg_gemm. */
+/* The launch configuration sg_gemm would use for TMA-legal A and B (no GPU
+ * work is queued).  Needs a current CUDA device; returns the same codes as
+ * sg_gemm. */
 typedef struct {
     int32_t block_m;       /* output tile rows (128) */
     int32_t block_n;       /* output tile columns */

@@ -96,12 +96,16 @@ int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
             return SG_ERR_ALIAS;
     }
     if (bias && overlap(C, c_span, bias, static_cast<uint64_t>(N) * 4)) return SG_ERR_ALIAS;
-    if (K > 0) {
-        if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15)) return SG_ERR_ALIGN;
-        // a single row has no pitch to align
-        if ((M > 1 && (lda * 2) % 16) || (K > 1 && (ldb * 2) % 16)) return SG_ERR_ALIGN;
-    }
+    // 16-bit elements must sit on 2-byte boundaries; anything coarser is
+    // handled (TMA when legal, element loads otherwise)
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 1) || (reinterpret_cast<uintptr_t>(B) & 1))) return SG_ERR_ALIGN;
     return SG_OK;
+}
+
+// An operand can be copied by TMA when its base is 16-byte aligned and its
+// row pitch is a multiple of 16 bytes (a single row has no pitch).
+bool tma_legal(const void* X, int64_t rows, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(X) & 15) == 0 && (rows <= 1 || (ld * 2) % 16 == 0);
 }
 
 int ensure_encode_fn() {
@@ -152,6 +156,7 @@ struct Plan {
     int tmem_cols = 0;
     int tma_store = 0;
     int epi_bufs = 1;
+    int a_tma = 1, b_tma = 1;  // operand copied by TMA (1) or by element loads (0)
 };
 
 int smem_for(int bn, int stages, int mode, int bufs) {
@@ -191,7 +196,9 @@ std::atomic<int> g_force_mode{[] {
 }()};
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype, const void* C, int64_t ldc,
-              int stages, Plan* pl) {
+              int stages, bool a_tma, bool b_tma, Plan* pl) {
+    pl->a_tma = a_tma ? 1 : 0;
+    pl->b_tma = b_tma ? 1 : 0;
     pl->m_blocks = cdiv(M, sg::BM);
     pl->k_chunks = cdiv(K, sg::BK);
     // Tile width: the widest of 256 / 192 / 128 that covers N as tightly as
@@ -220,6 +227,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
                    ? 3
                    : 1;
     if (const int f = g_force_mode.load(); f == 1 || (f >= 2 && pairable)) mode = f;
+    if (!a_tma || !b_tma) mode = 1;  // element-load staging runs in single-CTA mode
     pl->mode = mode;
     pl->cm = mode == 1 ? 1 : 2;
     const int cm = pl->cm;
@@ -350,27 +358,24 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
     }
 }
 
-}  // namespace
-
-extern "C" {
-
-int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
-            int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias, int stages, void* stream) {
-    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
-    if (rc != SG_OK) return rc;
-    if (M == 0 || N == 0) return SG_OK;
-    DevState* st = nullptr;
-    if ((rc = device_state(&st)) != SG_OK) return rc;
+// Plan, build the tensor maps and kernel parameters, and launch (shared by
+// both entry points; `st` supplies the device's attributes and status word).
+int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
+                    int stages, int64_t skip_load, cudaStream_t stream) {
+    const bool a_tma = tma_legal(A, M, lda);
+    const bool b_tma = tma_legal(B, K, ldb);
     Plan pl;
-    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, &pl)) != SG_OK) return rc;
+    int rc = make_plan(st, M, N, K, out_dtype, C, ldc, stages, a_tma, b_tma, &pl);
+    if (rc != SG_OK) return rc;
 
     alignas(64) CUtensorMap ta, tb, tc;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     std::memset(&tc, 0, sizeof(tc));
     if (K > 0) {
-        if ((rc = encode_2d(&ta, in_dtype, A, K, M, lda * 2, sg::BK, sg::BM)) != SG_OK) return rc;
-        if ((rc = encode_2d(&tb, in_dtype, B, N, K, ldb * 2, 64, sg::BK)) != SG_OK) return rc;
+        if (a_tma && (rc = encode_2d(&ta, in_dtype, A, K, M, lda * 2, sg::BK, sg::BM)) != SG_OK) return rc;
+        if (b_tma && (rc = encode_2d(&tb, in_dtype, B, N, K, ldb * 2, 64, sg::BK)) != SG_OK) return rc;
     }
     if (pl.tma_store) {
         const int oes = elem_bytes(out_dtype);
@@ -395,12 +400,31 @@ int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
     prm.bias = bias;
     prm.C = C;
     prm.ldc = ldc;
-    prm.status = st->status;
+    prm.status = st.status;
     prm.wait_limit_ns = g_wait_limit_ns.load();
-    prm.skip_load = g_skip_load.load();
+    prm.skip_load = skip_load;
+    prm.a_tma = pl.a_tma;
+    prm.b_tma = pl.b_tma;
+    prm.A = static_cast<const uint16_t*>(A);
+    prm.B = static_cast<const uint16_t*>(B);
+    prm.lda = lda;
+    prm.ldb = ldb;
+    return launch_plan(st, out_dtype, pl, ta, tb, tc, prm, stream);
+}
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return launch_plan(*st, out_dtype, pl, ta, tb, tc, prm, s);
+}  // namespace
+
+extern "C" {
+
+int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+            int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias, int stages, void* stream) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    DevState* st = nullptr;
+    if ((rc = device_state(&st)) != SG_OK) return rc;
+    return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                           g_skip_load.load(), static_cast<cudaStream_t>(stream));
 }
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages, int64_t ldc,
@@ -414,7 +438,7 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
     int rc = device_state(&st);
     if (rc != SG_OK) return rc;
     Plan pl;
-    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, &pl)) != SG_OK) return rc;
+    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, true, true, &pl)) != SG_OK) return rc;
     info->block_m = sg::BM;
     info->block_n = pl.bn;
     info->block_k = sg::BK;
@@ -543,48 +567,10 @@ int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     if (kNoallocScratchNeed > SG_NOALLOC_SCRATCH_BYTES) return SG_ERR_ARG;  // the need is fixed; never taken
     DevState* st = nullptr;
     if ((rc = noalloc_state(&st)) != SG_OK) return rc;
-    Plan pl;
-    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, &pl)) != SG_OK) return rc;
-
-    alignas(64) CUtensorMap ta, tb, tc;
-    std::memset(&ta, 0, sizeof(ta));
-    std::memset(&tb, 0, sizeof(tb));
-    std::memset(&tc, 0, sizeof(tc));
-    if (K > 0) {
-        if ((rc = encode_2d(&ta, in_dtype, A, K, M, lda * 2, sg::BK, sg::BM)) != SG_OK) return rc;
-        if ((rc = encode_2d(&tb, in_dtype, B, N, K, ldb * 2, 64, sg::BK)) != SG_OK) return rc;
-    }
-    if (pl.tma_store) {
-        const int oes = elem_bytes(out_dtype);
-        if ((rc = encode_2d(&tc, out_dtype, C, N, M, ldc * oes, 128 / oes, 32)) != SG_OK) return rc;
-    }
-
-    sg::Params prm;
-    std::memset(&prm, 0, sizeof(prm));
-    prm.M = static_cast<int32_t>(M);
-    prm.N = static_cast<int32_t>(N);
-    prm.K = static_cast<int32_t>(K);
-    prm.m_blocks = static_cast<int32_t>(pl.m_blocks);
-    prm.n_blocks = static_cast<int32_t>(pl.n_blocks);
-    prm.num_tiles = static_cast<int32_t>(pl.tiles);
-    prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
-    prm.stages = pl.stages;
-    prm.epi_bufs = pl.epi_bufs;
-    prm.group_m = kGroupM;
-    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, pl.mode == 3 ? 2 * sg::BM : sg::BM, pl.bn, true);
-    prm.epi = epilogue;
-    prm.tma_store = pl.tma_store;
-    prm.bias = bias;
-    prm.C = C;
-    prm.ldc = ldc;
-    prm.status = st->status;
-    prm.wait_limit_ns = g_wait_limit_ns.load();
-    prm.skip_load = -1;
-
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's word: clear it for this call
     if (cudaMemsetAsync(st->status, 0, sizeof(int), s) != cudaSuccess) return SG_ERR_CUDA;
-    return launch_plan(*st, out_dtype, pl, ta, tb, tc, prm, s);
+    return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages, -1, s);
 }
 
 int sg_gemm_noalloc_status(void* stream) {

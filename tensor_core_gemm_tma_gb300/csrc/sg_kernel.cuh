@@ -120,7 +120,64 @@ struct Params {
     int* status;
     uint64_t wait_limit_ns;
     int64_t skip_load;     // test hook: this global K-chunk index is never copied (-1: off)
+    // Operands without a TMA-legal layout (base not 16-byte aligned, or a row
+    // pitch that is not a multiple of 16 bytes) are copied by the producer
+    // warp with element loads instead (single-CTA mode only).
+    int32_t a_tma, b_tma;  // 1: copied by TMA, 0: by element loads
+    const uint16_t* A;     // 16-bit elements; used when a_tma == 0
+    const uint16_t* B;     // used when b_tma == 0
+    int64_t lda, ldb;
 };
+
+// Element-load staging of one A chunk (rows m0.., k0..k0+63) into the same
+// 128-byte-swizzled K-major layout the TMA box produces: row r at r * 128,
+// 16-byte chunk c of it at c ^ (r mod 8).  Out-of-range elements are
+// written as 0 (Tolk.Stage: a gate whose index fails copies 0).  Whole warp.
+__device__ __forceinline__ void copy_a_elements(uint32_t dst, const Params& p, int m0, int k0, int lane) {
+#pragma unroll 1
+    for (int c = lane; c < BM * 8; c += 32) {
+        const int r = c >> 3, ch = c & 7;
+        const int row = m0 + r;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k = k0 + ch * 8 + 2 * e;
+            const uint16_t* src = p.A + static_cast<int64_t>(row) * p.lda + k;
+            const uint32_t lo = (row < p.M && k < p.K) ? __ldg(src) : 0u;
+            const uint32_t hi = (row < p.M && k + 1 < p.K) ? __ldg(src + 1) : 0u;
+            w[e] = lo | (hi << 16);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + r * 128 + ((ch ^ (r & 7)) << 4)),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+    }
+}
+
+// The same for one B chunk (K rows k0..k0+63, columns n0..n0+ncols-1) into
+// the MN-major layout of the TMA boxes: 64-column box j at j * 8 KiB, K row
+// kr at kr * 128, 16-byte chunk c of it at c ^ (kr mod 8).
+__device__ __forceinline__ void copy_b_elements(uint32_t dst, const Params& p, int k0, int n0, int ncols, int lane) {
+    const int chunks = ncols / 8;  // 16-byte chunks per K row
+#pragma unroll 1
+    for (int c = lane; c < BK * chunks; c += 32) {
+        const int kr = c / chunks, cc = c - kr * chunks;
+        const int j = cc >> 3, ch = cc & 7;
+        const int k = k0 + kr;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = n0 + cc * 8 + 2 * e;
+            const uint16_t* src = p.B + static_cast<int64_t>(k) * p.ldb + n;
+            const uint32_t lo = (k < p.K && n < p.N) ? __ldg(src) : 0u;
+            const uint32_t hi = (k < p.K && n + 1 < p.N) ? __ldg(src + 1) : 0u;
+            w[e] = lo | (hi << 16);
+        }
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + j * B_CHUNK_BYTES + kr * 128 +
+                                                                     ((ch ^ (kr & 7)) << 4)),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+    }
+}
 
 // Linear cluster-tile index -> (row block of this CTA, column block), with a
 // grouped raster over cluster row blocks (CM row blocks each): group_m of
@@ -279,8 +336,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (warp == 0 && lane == 0) {
         if (p.k_chunks > 0) {
-            prefetch_tmap(&tmA);
-            prefetch_tmap(&tmB);
+            if (p.a_tma) prefetch_tmap(&tmA);
+            if (p.b_tma) prefetch_tmap(&tmB);
         }
         if (p.tma_store) prefetch_tmap(&tmC);
     }
@@ -299,7 +356,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp == 0 && MODE == 1 && !(p.a_tma && p.b_tma)) {
+        // ------------------------------------------------ element-load producer
+        // (an operand without a TMA-legal layout; the whole warp copies)
+        if (p.k_chunks > 0) {
+            uint32_t slot = 0, phase = 0;
+            uint32_t issued = 0, last_parity = 0;  // slots with TMA bytes in flight
+            const uint32_t tx = (p.a_tma ? A_STAGE_BYTES : 0) + (p.b_tma ? L::B_STAGE_BYTES : 0);
+            int64_t it = 0;
+            bool ok = true;
+            for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+                int mb, nb;
+                tile_coords<CM>(tile, p, rank, mb, nb);
+                for (int kc = 0; kc < p.k_chunks; ++kc, ++it) {
+                    const bool w = wait_bounded(empty_bar(slot), phase ^ 1u, abort_flag, p.status, p.wait_limit_ns,
+                                                SITE_PRODUCER_EMPTY);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it != p.skip_load) {
+                        const uint32_t sa = base + slot * L::STAGE_BYTES;
+                        if (lane == 0 && tx > 0) {
+                            mbar_expect_tx(full_bar(slot), tx);
+                            if (p.a_tma) tma_load_2d(sa, &tmA, full_bar(slot), kc * BK, mb * BM);
+                            if (p.b_tma) {
+#pragma unroll
+                                for (int j = 0; j < BN / 64; ++j)
+                                    tma_load_2d(sa + A_STAGE_BYTES + j * B_CHUNK_BYTES, &tmB, full_bar(slot),
+                                                nb * BN + j * 64, kc * BK);
+                            }
+                            issued |= 1u << slot;
+                            last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
+                        }
+                        if (!p.a_tma) copy_a_elements(sa, p, mb * BM, kc * BK, lane);
+                        if (!p.b_tma) copy_b_elements(sa + A_STAGE_BYTES, p, kc * BK, nb * BN, BN, lane);
+                        // the MMA reads these bytes through the async proxy
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(full_bar(slot));
+                    }
+                    if (++slot == static_cast<uint32_t>(stages)) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && lane == 0) {
+                for (int s = 0; s < stages; ++s)
+                    if ((issued >> s) & 1u) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
+            }
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0 && p.k_chunks > 0) {
             uint32_t slot = 0, phase = 0;

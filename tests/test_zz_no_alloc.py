@@ -59,7 +59,11 @@ def test_noalloc_matches_sg_gemm_twice(M, N, K, in_dt, out_dt, epi):
 
 
 def test_noalloc_rejects_like_sg_gemm():
+    """Host-side checks are sg_gemm's.  Only arguments that are rejected on
+    the host before any CUDA call are used here (the pointers are not real
+    device memory): an A that is not aligned to its 2-byte elements, an
+    unknown epilogue, a negative size."""
     lib = _noalloc_lib()
-    # host-side checks are sg_gemm's: misaligned A, then an unknown epilogue
-    assert lib.sg_gemm_noalloc(64, 64, 64, 0x10002, 64, 0x20000, 64, 0x400000, 64, 1, 0, 0, None, 0, None) == -5
+    assert lib.sg_gemm_noalloc(64, 64, 64, 0x10001, 64, 0x20000, 64, 0x400000, 64, 1, 0, 0, None, 0, None) == -5
     assert lib.sg_gemm_noalloc(64, 64, 64, 0x10000, 64, 0x20000, 64, 0x400000, 64, 1, 0, 9, None, 0, None) == -2
+    assert lib.sg_gemm_noalloc(-1, 64, 64, 0x10000, 64, 0x20000, 64, 0x400000, 64, 1, 0, 0, None, 0, None) == -1
