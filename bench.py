@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg (profiling runs)")
     ap.add_argument("--no-secondary", action="store_true", help="skip the other-workload summary")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--no-tune", action="store_true",
+                    help="use the planner's heuristic instead of tuning the configuration first (sg_tune)")
     return ap.parse_args()
 
 
@@ -103,10 +105,11 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -118,7 +121,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.INTERVAL_MS)], stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -242,19 +245,27 @@ def config_of(w, plan):
          "l2": "flushed between timed steps (256 MiB write outside the timed events)",
          "description": w.description}
     if plan:
-        c["tile"] = f"{plan['block_m']}x{plan['block_n']}x{plan['block_k']}"
+        rows = plan["block_m"] * (2 if plan.get("pair_mma") else 1)
+        c["tile"] = f"{rows}x{plan['block_n']}x{plan['block_k']}"
         c["stages"] = plan["stages"]
         c["grid"] = plan["grid"]
+        c["kernel_mode"] = ("paired MMA (cta_group::2)" if plan.get("pair_mma") else
+                            "CTA pair, B multicast" if plan.get("cluster_m") == 2 else "single CTA")
+        c["raster_group_m"] = plan.get("group_m")
+        c["tuned"] = plan.get("tuned", False)
     return c
 
 
-def measure(sg, w, device, stream, steps, warmup, stages, inputs=None):
+def measure(sg, w, device, stream, steps, warmup, stages, inputs=None, tune=True):
     import torch
     A_h, B_h, bias_h = inputs if inputs is not None else device_inputs(w, device)
     A = A_h.to(device)
     B = B_h.to(device)
     bias = None if bias_h is None else bias_h.to(device)
     C = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), device=device)
+    if tune and stages == 0:
+        # the library's own tuner picks the configuration (outside the timed steps)
+        sg.tune(A, B, epilogue=w.epilogue, bias=bias, out=C, stream=stream)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def call():
@@ -304,6 +315,23 @@ def measure_e2e(sg, w, host_inputs, device, stream, steps, stages):
         h2d += bias_p.numel() * 4
     d2h = out_h.numel() * out_h.element_size()
     return sum(ms) / len(ms), h2d, d2h
+
+
+def max_over_ranks(value: float, pg=None, device=None) -> float:
+    """The largest of every rank's `value` (the job is as slow as its slowest
+    replica).  With no process group: the value itself."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, world: int, steps: int, max_sum_ms: float) -> float:
+    """Every rank runs the same workload (replicas): total FLOPs of all
+    ranks over the slowest rank's summed step time."""
+    return flops_per_step * world * steps / (max_sum_ms * 1e-3) / 1e12
 
 
 def roofline_of(w, ms, peaks, traffic):
@@ -357,16 +385,13 @@ def main():
     with clocks:
         barrier()
         times, host_inputs, dev_tensors = measure(sg, w, device, stream, args.steps, args.warmup, args.stages,
-                                                  inputs=host_inputs)
+                                                  inputs=host_inputs, tune=not args.no_tune)
         barrier()
-    sum_ms = sum(times)
-    if pg is not None:
-        t = torch.tensor([sum_ms], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        sum_ms = float(t.item())
+    sum_ms = max_over_ranks(sum(times), pg, device)
     ms = sum_ms / len(times)
-    value = w.flops * world * len(times) / (sum_ms * 1e-3) / 1e12
+    value = whole_job_tflops(w.flops, world, len(times), sum_ms)
     plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages)
+    plan["tuned"] = (not args.no_tune) and args.stages == 0
 
     e2e = None
     if not args.no_e2e:
@@ -396,7 +421,7 @@ def main():
         sec = []
         for name in ("relu4096_f16", "swin4k_proj_f16"):
             ws = gemm_inputs.WORKLOADS[name]
-            t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0)
+            t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=not args.no_tune)
             del dt
             m2 = sum(t2) / len(t2)
             sec.append({"workload": name, "ms_per_step": m2, "TFLOP/s": ws.flops / (m2 * 1e-3) / 1e12,

@@ -142,11 +142,40 @@ typedef struct {
                               with the paired MMA; 0: one CTA per 128-row tile
                               (with cluster_m 2: the pair shares each B tile by
                               multicast) */
-    int32_t reserved[3];
+    int32_t group_m;       /* cluster row blocks swept together by the tile raster */
+    int32_t reserved[2];
 } sg_plan_info;
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,
             int64_t ldc, const void* C, sg_plan_info* info);
+
+/*
+ * sg_tune -- times every launch configuration that fits this problem (tile
+ * width, kernel mode, ring depth, raster group) on the
+ * caller's operands, on `stream`, and keeps the fastest for later sg_gemm
+ * and sg_plan calls with the same key (device, M, N, K, types, epilogue, and
+ * whether A, B and C are TMA-legal).  This is gizml:tile's "tune": each
+ * configuration is measured once and the choice cached; every configuration
+ * computes the same bits (the same products summed in the same K order), so
+ * tuning never changes a result.  C is written several times (the kernel
+ * never reads C); arguments are checked as by sg_gemm (stages is not an
+ * argument: ring depth is tuned).  Blocks until the measurements finish.
+ * `best` and `best_ms` (either may be NULL) receive the chosen plan and its
+ * time per call.  An explicit `stages` in a later sg_gemm call still wins.
+ */
+int sg_tune(int64_t M, int64_t N, int64_t K,
+            const void* A, int64_t lda,
+            const void* B, int64_t ldb,
+            void* C, int64_t ldc,
+            int in_dtype, int out_dtype, int epilogue,
+            const float* bias, void* stream,
+            sg_plan_info* best, float* best_ms);
+
+/* Forgets every tuned configuration; returns how many there were. */
+int sg_tune_clear(void);
+
+/* Tuned configurations currently cached. */
+int sg_tune_count(void);
 
 /* Waits for `stream`, then returns SG_ERR_TIMEOUT if any kernel of this
  * library on the current device gave up on a wait since the last call (and

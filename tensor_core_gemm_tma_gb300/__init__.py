@@ -44,7 +44,7 @@ class SgError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "block_n", "block_k", "stages", "max_stages", "tiles", "grid", "threads", "smem_bytes",
-        "tmem_columns", "tma_store", "cluster_m", "pair_mma")] + [("reserved", ctypes.c_int32 * 3)]
+        "tmem_columns", "tma_store", "cluster_m", "pair_mma", "group_m")] + [("reserved", ctypes.c_int32 * 2)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
@@ -80,6 +80,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.sg_strerror.argtypes = [i32]
         lib.sg_version.restype = i32
         lib.sg_version.argtypes = []
+        lib.sg_tune.restype = i32
+        lib.sg_tune.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, vp,
+                                ctypes.POINTER(PlanInfo), ctypes.POINTER(ctypes.c_float)]
+        lib.sg_tune_clear.restype = i32
+        lib.sg_tune_clear.argtypes = []
+        lib.sg_tune_count.restype = i32
+        lib.sg_tune_count.argtypes = []
         lib.sg_test_set_skip_load.restype = i32
         lib.sg_test_set_skip_load.argtypes = [i64]
         lib.sg_test_set_tile_n.restype = i32
@@ -200,6 +207,34 @@ def plan(M: int, N: int, K: int, in_dtype, out_dtype, epilogue: str = "none", st
                                 int(stages), N if ldc is None else ldc, C_ptr, ctypes.byref(info))
     _check(rc)
     return info.as_dict()
+
+
+def tune(A, B, out_dtype=None, epilogue: str = "none", bias=None, out=None, stream=None):
+    """Measure every launch configuration that fits C = epilogue(A @ B) on
+    these operands and keep the fastest for later calls with the same
+    shapes, types and layouts (gizml:tile, "tune").  Returns (plan dict,
+    milliseconds per call).  Every configuration computes the same bits."""
+    torch = _torch()
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    info = PlanInfo()
+    ms = ctypes.c_float(0.0)
+    bptr = None if bias is None else bias.data_ptr()
+    rc = load_library().sg_tune(M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), out.data_ptr(),
+                                _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype), EPILOGUES[epilogue], bptr,
+                                _stream_ptr(stream, A.device).value, ctypes.byref(info), ctypes.byref(ms))
+    _check(rc)
+    return info.as_dict(), float(ms.value)
+
+
+def tune_clear() -> int:
+    return int(load_library().sg_tune_clear())
+
+
+def tune_count() -> int:
+    return int(load_library().sg_tune_count())
 
 
 def device_status(stream=None) -> int:

@@ -8,11 +8,15 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "sg_kernel.cuh"
 #include "stage_gemm.h"
@@ -145,8 +149,24 @@ int device_state(DevState** out) {
     return SG_OK;
 }
 
+// A launch configuration chosen by sg_tune (or forced): every field
+// non-zero overrides the planner's heuristic.
+struct Choice {
+    int bn = 0, mode = 0, stages = 0, group_m = 0;
+};
+
+// Tuning cache: the fastest configuration measured for each problem key.
+using TuneKey = std::tuple<int, int64_t, int64_t, int64_t, int, int, int, int, int, int>;
+std::map<TuneKey, Choice> g_tuned;
+
+TuneKey tune_key(int dev, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epi, bool a_tma,
+                 bool b_tma, bool c_tma) {
+    return TuneKey(dev, M, N, K, in_dtype, out_dtype, epi, a_tma, b_tma, c_tma);
+}
+
 struct Plan {
     int bn = 128;
+    int group_m = 8;
     int mode = 1;  // 1: single CTA, 2: CTA pairs sharing B by multicast, 3: paired MMA
     int cm = 1;    // CTAs per cluster along M
     int stages = 0, max_stages = 0;
@@ -155,22 +175,21 @@ struct Plan {
     int smem = 0;
     int tmem_cols = 0;
     int tma_store = 0;
-    int epi_bufs = 1;
     int a_tma = 1, b_tma = 1;  // operand copied by TMA (1) or by element loads (0)
 };
 
-int smem_for(int bn, int stages, int mode, int bufs) {
+int smem_for(int bn, int stages, int mode) {
     if (mode == 3) {  // each CTA stages half of B
         switch (bn) {
-            case 128: return sg::Layout<128, 64>::smem_bytes(stages, bufs);
-            case 256: return sg::Layout<256, 128>::smem_bytes(stages, bufs);
+            case 128: return sg::Layout<128, 64>::smem_bytes(stages);
+            case 256: return sg::Layout<256, 128>::smem_bytes(stages);
             default: return -1;
         }
     }
     switch (bn) {
-        case 128: return sg::Layout<128>::smem_bytes(stages, bufs);
-        case 192: return sg::Layout<192>::smem_bytes(stages, bufs);
-        case 256: return sg::Layout<256>::smem_bytes(stages, bufs);
+        case 128: return sg::Layout<128>::smem_bytes(stages);
+        case 192: return sg::Layout<192>::smem_bytes(stages);
+        case 256: return sg::Layout<256>::smem_bytes(stages);
         default: return -1;
     }
 }
@@ -196,7 +215,7 @@ std::atomic<int> g_force_mode{[] {
 }()};
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype, const void* C, int64_t ldc,
-              int stages, bool a_tma, bool b_tma, Plan* pl) {
+              int stages, bool a_tma, bool b_tma, Plan* pl, const Choice* choice = nullptr) {
     pl->a_tma = a_tma ? 1 : 0;
     pl->b_tma = b_tma ? 1 : 0;
     pl->m_blocks = cdiv(M, sg::BM);
@@ -217,7 +236,9 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
         }
     }
     if (forced_bn()) bn = forced_bn();
+    if (choice && choice->bn) bn = choice->bn;
     pl->bn = bn;
+    pl->group_m = (choice && choice->group_m) ? choice->group_m : kGroupM;
     pl->n_blocks = cdiv(N, bn);
     // Pairs of CTAs compute 256-row tiles with the paired MMA when the
     // problem is large and the K loop long enough for operand traffic to
@@ -227,29 +248,22 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
                    ? 3
                    : 1;
     if (const int f = g_force_mode.load(); f == 1 || (f >= 2 && pairable)) mode = f;
+    if (choice && choice->mode && (choice->mode == 1 || pairable)) mode = choice->mode;
     if (!a_tma || !b_tma) mode = 1;  // element-load staging runs in single-CTA mode
     pl->mode = mode;
     pl->cm = mode == 1 ? 1 : 2;
     const int cm = pl->cm;
     pl->tiles = cdiv(pl->m_blocks, cm) * pl->n_blocks;  // cluster tiles
-    // One staging buffer per epilogue warp: measured on the skinny-K
-    // projection, a sixth ring stage is worth more than a second buffer.
-    // STAGE_GEMM_EPI_BUFS=2 (read at load) gives each warp two, for tuning.
-    static const int env_bufs = [] {
-        const char* e = std::getenv("STAGE_GEMM_EPI_BUFS");
-        return (e && std::atoi(e) == 2) ? 2 : 1;
-    }();
-    const int bufs = env_bufs;
-    pl->epi_bufs = bufs;
     int maxs = 0;
     for (int s = 1; s <= SG_MAX_STAGES; ++s)
-        if (smem_for(bn, s, mode, bufs) <= st.smem_optin) maxs = s;
+        if (smem_for(bn, s, mode) <= st.smem_optin) maxs = s;
     pl->max_stages = maxs;
     if (maxs == 0) return SG_ERR_STAGES;
+    if (stages == 0 && choice && choice->stages) stages = std::min(choice->stages, maxs);
     if (stages == 0) stages = maxs;
     if (stages > maxs) return SG_ERR_STAGES;
     pl->stages = stages;
-    pl->smem = smem_for(bn, stages, mode, bufs);
+    pl->smem = smem_for(bn, stages, mode);
     pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for
     // it; keep one persistent CTA per SM by asking for more than half of the
@@ -360,14 +374,59 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
 
 // Plan, build the tensor maps and kernel parameters, and launch (shared by
 // both entry points; `st` supplies the device's attributes and status word).
+void fill_info(const Plan& pl, sg_plan_info* info) {
+    std::memset(info, 0, sizeof(*info));
+    info->block_m = sg::BM;
+    info->block_n = pl.bn;
+    info->block_k = sg::BK;
+    info->stages = pl.stages;
+    info->max_stages = pl.max_stages;
+    info->tiles = static_cast<int32_t>(pl.tiles);
+    info->grid = pl.grid;
+    info->threads = sg::NUM_THREADS;
+    info->smem_bytes = pl.smem;
+    info->tmem_columns = pl.tmem_cols;
+    info->tma_store = pl.tma_store;
+    info->cluster_m = pl.cm;
+    info->pair_mma = pl.mode == 3 ? 1 : 0;
+    info->group_m = pl.group_m;
+}
+
+bool c_tma_legal(const void* C, int64_t M, int64_t ldc, int out_dtype) {
+    return (reinterpret_cast<uintptr_t>(C) & 15) == 0 && (M == 1 || (ldc * elem_bytes(out_dtype)) % 16 == 0);
+}
+
+int current_device() {
+    int dev = 0;
+    return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
+// The tuned configuration for this problem, if sg_tune measured one.
+bool lookup_tuned(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epi, bool a_tma, bool b_tma,
+                  bool c_tma, Choice* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_tuned.empty()) return false;
+    auto it = g_tuned.find(tune_key(current_device(), M, N, K, in_dtype, out_dtype, epi, a_tma, b_tma, c_tma));
+    if (it == g_tuned.end()) return false;
+    *out = it->second;
+    return true;
+}
+
 int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
-                    int stages, int64_t skip_load, cudaStream_t stream) {
+                    int stages, int64_t skip_load, cudaStream_t stream, const Choice* forced = nullptr,
+                    Plan* used = nullptr) {
     const bool a_tma = tma_legal(A, M, lda);
     const bool b_tma = tma_legal(B, K, ldb);
+    Choice tuned;
+    const Choice* choice = forced;
+    if (!choice && lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, a_tma, b_tma,
+                                c_tma_legal(C, M, ldc, out_dtype), &tuned))
+        choice = &tuned;
     Plan pl;
-    int rc = make_plan(st, M, N, K, out_dtype, C, ldc, stages, a_tma, b_tma, &pl);
+    int rc = make_plan(st, M, N, K, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice);
     if (rc != SG_OK) return rc;
+    if (used) *used = pl;
 
     alignas(64) CUtensorMap ta, tb, tc;
     std::memset(&ta, 0, sizeof(ta));
@@ -392,8 +451,7 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.num_tiles = static_cast<int32_t>(pl.tiles);
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
-    prm.epi_bufs = pl.epi_bufs;
-    prm.group_m = kGroupM;
+    prm.group_m = pl.group_m;
     prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, pl.mode == 3 ? 2 * sg::BM : sg::BM, pl.bn, true);
     prm.epi = epilogue;
     prm.tma_store = pl.tma_store;
@@ -438,21 +496,100 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
     int rc = device_state(&st);
     if (rc != SG_OK) return rc;
     Plan pl;
-    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, true, true, &pl)) != SG_OK) return rc;
-    info->block_m = sg::BM;
-    info->block_n = pl.bn;
-    info->block_k = sg::BK;
-    info->stages = pl.stages;
-    info->max_stages = pl.max_stages;
-    info->tiles = static_cast<int32_t>(pl.tiles);
-    info->grid = pl.grid;
-    info->threads = sg::NUM_THREADS;
-    info->smem_bytes = pl.smem;
-    info->tmem_columns = pl.tmem_cols;
-    info->tma_store = pl.tma_store;
-    info->cluster_m = pl.cm;
-    info->pair_mma = pl.mode == 3 ? 1 : 0;
+    Choice tuned;
+    const bool have = lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, true, true,
+                                   c_tma_legal(C, M, ldc, out_dtype), &tuned);
+    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, true, true, &pl, have ? &tuned : nullptr)) != SG_OK)
+        return rc;
+    fill_info(pl, info);
     return SG_OK;
+}
+
+int sg_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+            int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias, void* stream,
+            sg_plan_info* best, float* best_ms) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, 0);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    DevState* st = nullptr;
+    if ((rc = device_state(&st)) != SG_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool a_tma = tma_legal(A, M, lda), b_tma = tma_legal(B, K, ldb);
+    const bool c_tma = c_tma_legal(C, M, ldc, out_dtype);
+    const int64_t m_blocks = cdiv(M, sg::BM);
+
+    // the configurations that fit this problem
+    std::vector<Choice> cands;
+    for (int bn : {128, 192, 256}) {
+        if (bn > 128 && N <= bn - 64) continue;  // a tile mostly past N
+        for (int mode : {1, 2, 3}) {
+            if (mode > 1 && ((bn / 64) % 2 != 0 || m_blocks < 2 || !a_tma || !b_tma)) continue;
+            for (int g : {4, 8, 16}) {
+                Choice c;
+                c.bn = bn;
+                c.mode = mode;
+                c.group_m = g;
+                // the raster only matters when there are more tiles than CTAs
+                if (g != 8 && m_blocks * cdiv(N, bn) <= st->sm_count) continue;
+                cands.push_back(c);
+            }
+        }
+    }
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return SG_ERR_CUDA;
+    float best_t = -1.0f;
+    Choice best_c;
+    Plan best_p;
+    constexpr int kReps = 3;
+    for (const Choice& c : cands) {
+        Plan pl;
+        // one untimed run (sets kernel attributes, warms caches), then the reps
+        rc = plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, 0, -1, s, &c,
+                             &pl);
+        if (rc != SG_OK) continue;
+        float t_min = -1.0f;
+        for (int r = 0; r < kReps && rc == SG_OK; ++r) {
+            if (cudaEventRecord(e0, s) != cudaSuccess) rc = SG_ERR_CUDA;
+            if (rc == SG_OK)
+                rc = plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, 0, -1,
+                                     s, &c);
+            if (rc == SG_OK && cudaEventRecord(e1, s) != cudaSuccess) rc = SG_ERR_CUDA;
+            if (rc == SG_OK && cudaEventSynchronize(e1) != cudaSuccess) rc = SG_ERR_CUDA;
+            float ms = 0.0f;
+            if (rc == SG_OK && cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) rc = SG_ERR_CUDA;
+            if (rc == SG_OK && (t_min < 0.0f || ms < t_min)) t_min = ms;
+        }
+        if (rc != SG_OK) break;
+        if (best_t < 0.0f || t_min < best_t) {
+            best_t = t_min;
+            best_c = c;
+            best_p = pl;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (rc != SG_OK) return rc;
+    if (best_t < 0.0f) return SG_ERR_STAGES;  // nothing fitted
+    best_c.stages = best_p.stages;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_tuned[tune_key(current_device(), M, N, K, in_dtype, out_dtype, epilogue, a_tma, b_tma, c_tma)] = best_c;
+    }
+    if (best) fill_info(best_p, best);
+    if (best_ms) *best_ms = best_t;
+    return SG_OK;
+}
+
+int sg_tune_clear(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int n = static_cast<int>(g_tuned.size());
+    g_tuned.clear();
+    return n;
+}
+
+int sg_tune_count(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return static_cast<int>(g_tuned.size());
 }
 
 int sg_device_status(void* stream) {

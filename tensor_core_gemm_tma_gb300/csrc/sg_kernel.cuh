@@ -75,8 +75,7 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int B_CHUNK_BYTES = BK * 64 * 2;  // one TMA box of B: 64 K-rows x 64 N-columns
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int EPI_BUF_BYTES = 32 * 128;     // one staging buffer: 32 rows x 128 bytes
-constexpr int MAX_EPI_BUFS = 2;             // staging buffers per epilogue warp (1 or 2)
+constexpr int EPI_BUF_BYTES = 32 * 128;     // one warp's staging buffer: 32 rows x 128 bytes
 constexpr int TMEM_COLS = 512;              // the whole tensor memory of the SM
 constexpr int MAX_ACC = 4;                  // accumulators in flight (512 / 128)
 constexpr int SMEM_ALIGN = 1024;            // 128-byte swizzle atoms repeat every 1024 bytes
@@ -96,20 +95,17 @@ struct Layout {
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int ACC = (TMEM_COLS / BN) < MAX_ACC ? (TMEM_COLS / BN) : MAX_ACC;
     static __host__ __device__ constexpr int epi_offset(int stages) { return stages * STAGE_BYTES; }
-    static __host__ __device__ constexpr int bar_offset(int stages, int bufs) {
-        return epi_offset(stages) + EPI_WARPS * bufs * EPI_BUF_BYTES;
+    static __host__ __device__ constexpr int bar_offset(int stages) {
+        return epi_offset(stages) + EPI_WARPS * EPI_BUF_BYTES;
     }
     // dynamic shared memory to request (with slack for aligning the base)
-    static __host__ __device__ constexpr int smem_bytes(int stages, int bufs) {
-        return bar_offset(stages, bufs) + BAR_AREA + SMEM_ALIGN;
-    }
+    static __host__ __device__ constexpr int smem_bytes(int stages) { return bar_offset(stages) + BAR_AREA + SMEM_ALIGN; }
 };
 
 struct Params {
     int32_t M, N, K;
     int32_t m_blocks, n_blocks, num_tiles, k_chunks;  // num_tiles counts cluster tiles (CM row blocks each)
     int32_t stages;
-    int32_t epi_bufs;      // staging buffers per epilogue warp (1 or 2)
     int32_t group_m;       // tile raster: group_m row-blocks swept together for L2 reuse
     uint32_t idesc;        // tcgen05 instruction descriptor
     int32_t epi;           // SG_EPI_*
@@ -306,8 +302,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     const int stages = p.stages;
 
-    const int epi_bufs = p.epi_bufs;
-    const uint32_t bar0 = base + L::bar_offset(stages, epi_bufs);
+    const uint32_t bar0 = base + L::bar_offset(stages);
     // barrier slots: full[0..7], empty[8..15], tmem_full[16..19], tmem_empty[20..23], drain[24]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (SG_MAX_STAGES + s); };
@@ -315,7 +310,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + MAX_ACC + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * SG_MAX_STAGES + 2 * MAX_ACC);
     uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(gbase + L::bar_offset(stages, epi_bufs) + 8 * (2 * SG_MAX_STAGES + 2 * MAX_ACC + 1));
+        reinterpret_cast<uint32_t*>(gbase + L::bar_offset(stages) + 8 * (2 * SG_MAX_STAGES + 2 * MAX_ACC + 1));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -543,8 +538,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;                   // the tensor-memory lane quarter this warp may read
         constexpr int SPLIT = EPI_WARPS / 4;      // warps sharing a quarter
         const int part = e / 4;                   // which of them: takes column chunks part, part+SPLIT, ...
-        const uint32_t buf0 = base + L::epi_offset(stages) + e * epi_bufs * EPI_BUF_BYTES;
-        uint32_t buf_i = 0;
+        const uint32_t buf = base + L::epi_offset(stages) + e * EPI_BUF_BYTES;
         uint32_t ab = 0, aph = 0;
         for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
             int mb, nb;
@@ -591,15 +585,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (p.tma_store) {
                     if (row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
-                        const uint32_t buf = buf0 + (buf_i % static_cast<uint32_t>(epi_bufs)) * EPI_BUF_BYTES;
-                        // the store that last used this buffer has read it
-                        if (lane == 0) {
-                            if (epi_bufs == 1) {
-                                bulk_wait_group_read<0>();
-                            } else {
-                                bulk_wait_group_read<1>();
-                            }
-                        }
+                        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
                         __syncwarp();
                         const uint32_t rowaddr = buf + lane * 128;
 #pragma unroll
@@ -630,7 +616,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tma_store_2d(&tmC, buf, col0, row0);
                             bulk_commit_group();
                         }
-                        ++buf_i;
                     }
                 } else if (row < p.M) {
 #pragma unroll
