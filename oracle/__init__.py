@@ -12,7 +12,11 @@ Citations (page title and section):
   * gizml:tile, "Tile.run" example, "Tile.relu", "Tile.add": the fused ReLU and
     the broadcast per-column bias.
   * gizml:tile, "Tile.to": one final round to the storage type (RNE).
-  * gizml:tile, "Program.fold": an empty K range returns the init (zeros).
+  * gizml:tile, "Program.fold": an empty K range returns the init (zeros,
+    or the residual R when one is given).
+  * d4r, rrswin_enc2_epilogues.md, "Shape of the whole MLP band": the
+    back-projection's MMA takes the previous accumulator as its C input,
+    D = A . B + C -- the residual R added to the sum before bias and ReLU.
 
 Parity pins for every function here live in ``tests/test_oracle_pins.py``.
 """
@@ -63,6 +67,12 @@ def _load():
         lib.orc_encode.argtypes = [i32, ctypes.c_double]
         lib.orc_gemm.restype = i32
         lib.orc_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, i32, vp, i32, vp, i64, dp, dp, i32]
+        lib.orc_gemm_residual.restype = i32
+        lib.orc_gemm_residual.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i32, i64, i32, i32, vp, i32, vp, i64,
+                                          dp, dp, i32]
+        lib.orc_gemm_residual_at.restype = i32
+        lib.orc_gemm_residual_at.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i32, i64, i32, i32, vp, i32, i64,
+                                             vp, vp, vp, dp, dp, i32]
         lib.orc_gemm_at.restype = i32
         lib.orc_gemm_at.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, i32, vp, i32, i64, vp, vp, vp, dp, dp,
                                     i32]
@@ -115,15 +125,29 @@ def _ld(X) -> int:
     return max(X.strides[0] // 2, X.shape[1]) if X.size > 0 and X.shape[0] > 1 else X.shape[1]
 
 
+def _residual(R_bits, r_dtype, N):
+    if R_bits is None:
+        return None, _DT["f32"], 0
+    if r_dtype is None:
+        raise ValueError("r_dtype is required with a residual")
+    R = np.asarray(R_bits)
+    if R.dtype != _NP_BITS[r_dtype] or R.ndim != 2 or (R.shape[1] > 1 and R.strides[1] != R.itemsize):
+        raise ValueError("R must be a row-major bit matrix of r_dtype")
+    ldr = max(R.strides[0] // R.itemsize, R.shape[1]) if R.shape[0] > 1 else R.shape[1]
+    return R, _DT[r_dtype], ldr
+
+
 def gemm(A_bits: np.ndarray, B_bits: np.ndarray, in_dtype: str, out_dtype: str, epilogue: str = "none",
          bias: np.ndarray | None = None, K: int | None = None, N: int | None = None, threads: int | None = None,
-         C_init: np.ndarray | None = None):
+         C_init: np.ndarray | None = None, R_bits: np.ndarray | None = None, r_dtype: str | None = None):
     """Full product.  A_bits is M x lda (uint16), B_bits is K x ldb (uint16);
     the logical K and N default to the arrays' widths (pass them to leave
-    ld padding unread).  Returns (C_bits, C_exact, S): C_bits is M x ldc in
-    the output's bit type (ldc = C_init's width, whose padding is kept
-    untouched; else N), C_exact the fp64 value before the final rounding and
-    S the sum of |a_ik b_kj|, both M x N."""
+    ld padding unread).  R_bits (M x ldr, of storage type r_dtype) is an
+    optional residual added to the sum before bias and ReLU.  Returns
+    (C_bits, C_exact, S): C_bits is M x ldc in the output's bit type (ldc =
+    C_init's width, whose padding is kept untouched; else N), C_exact the
+    fp64 value before the final rounding and S the sum of |a_ik b_kj|, both
+    M x N."""
     _check_operands(A_bits, B_bits, K)
     M = A_bits.shape[0]
     K = A_bits.shape[1] if K is None else int(K)
@@ -140,8 +164,10 @@ def gemm(A_bits: np.ndarray, B_bits: np.ndarray, in_dtype: str, out_dtype: str, 
     exact = np.empty((M, N), dtype=np.float64)
     S = np.empty((M, N), dtype=np.float64)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
-    rc = _load().orc_gemm(M, N, K, _ptr(A_bits), lda, _ptr(B_bits), ldb, _DT[in_dtype], _EPI[epilogue], _ptr(b),
-                          _DT[out_dtype], _ptr(C), ldc, _ptr(exact), _ptr(S), _threads(threads))
+    R, rdt, ldr = _residual(R_bits, r_dtype, N)
+    rc = _load().orc_gemm_residual(M, N, K, _ptr(A_bits), lda, _ptr(B_bits), ldb, _ptr(R), rdt, ldr, _DT[in_dtype],
+                                   _EPI[epilogue], _ptr(b), _DT[out_dtype], _ptr(C), ldc, _ptr(exact), _ptr(S),
+                                   _threads(threads))
     if rc != 0:
         raise ValueError(f"orc_gemm rejected its arguments (rc={rc})")
     return C, exact, S
@@ -149,7 +175,7 @@ def gemm(A_bits: np.ndarray, B_bits: np.ndarray, in_dtype: str, out_dtype: str, 
 
 def gemm_at(A_bits: np.ndarray, B_bits: np.ndarray, rows, cols, in_dtype: str, out_dtype: str,
             epilogue: str = "none", bias: np.ndarray | None = None, K: int | None = None, N: int | None = None,
-            threads: int | None = None):
+            threads: int | None = None, R_bits: np.ndarray | None = None, r_dtype: str | None = None):
     """The same definition at the positions (rows[t], cols[t]) only.
     Returns (C_bits, C_exact, S) as 1-D arrays over t."""
     _check_operands(A_bits, B_bits, K)
@@ -165,9 +191,10 @@ def gemm_at(A_bits: np.ndarray, B_bits: np.ndarray, rows, cols, in_dtype: str, o
     exact = np.empty(n, dtype=np.float64)
     S = np.empty(n, dtype=np.float64)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
-    rc = _load().orc_gemm_at(M, N, K, _ptr(A_bits), _ld(A_bits), _ptr(B_bits), _ld(B_bits),
-                             _DT[in_dtype], _EPI[epilogue], _ptr(b), _DT[out_dtype], n, _ptr(r), _ptr(c),
-                             _ptr(bits), _ptr(exact), _ptr(S), _threads(threads))
+    R, rdt, ldr = _residual(R_bits, r_dtype, N)
+    rc = _load().orc_gemm_residual_at(M, N, K, _ptr(A_bits), _ld(A_bits), _ptr(B_bits), _ld(B_bits), _ptr(R), rdt,
+                                      ldr, _DT[in_dtype], _EPI[epilogue], _ptr(b), _DT[out_dtype], n, _ptr(r),
+                                      _ptr(c), _ptr(bits), _ptr(exact), _ptr(S), _threads(threads))
     if rc != 0:
         raise ValueError(f"orc_gemm_at rejected its arguments (rc={rc})")
     return bits.astype(_NP_BITS[out_dtype]), exact, S
@@ -183,10 +210,16 @@ def ulp(values: np.ndarray, dtype: str) -> np.ndarray:
     return np.ldexp(1.0, (e - fbits).astype(np.int64))
 
 
-def tolerance(S: np.ndarray, C_ref_value: np.ndarray, out_dtype: str) -> np.ndarray:
+def tolerance(S: np.ndarray, C_ref_value: np.ndarray, out_dtype: str, added=None) -> np.ndarray:
     """The parity bound: 1e-3 * sum|a b| + 1e-5, plus one ulp of the rounded
-    reference for 16-bit outputs."""
+    reference for 16-bit outputs.  `added` (|R| + |bias| per element) covers
+    the fp32 additions of a residual and a bias to the fp32 accumulator: each
+    rounds by at most half an fp32 ulp of its result, which is within
+    2^-24 * (|sum| + |R| + |bias|); the |sum| part lies inside 1e-3 * S, the
+    rest is 2^-23 * added."""
     tol = 1e-3 * np.asarray(S, dtype=np.float64) + 1e-5
+    if added is not None:
+        tol = tol + 2.0 ** -23 * np.abs(np.asarray(added, dtype=np.float64))
     if out_dtype in ("f16", "bf16"):
         tol = tol + ulp(C_ref_value, out_dtype)
     return tol

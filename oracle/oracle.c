@@ -31,6 +31,13 @@
  *     overflow to +-infinity, NaN stays NaN.
  *   - Empty K: gizml:tile, "Program.fold" -- a fold with no trips returns its
  *     init, so K = 0 gives C = epilogue(0 [+ bias]).
+ *   - Residual: the Swin-layer MLP band (d4r, rrswin_enc2_epilogues.md,
+ *     "Shape of the whole MLP band") ends with a back-projection whose MMA
+ *     takes the previous accumulator as its C input, D = A . B + C.  With a
+ *     residual R (M x N, in a storage type) the sum becomes
+ *     s_ij = R_ij + sum_k a_ik b_kj, before the bias and the ReLU: the
+ *     fold starts from R instead of zeros (gizml:tile, "Program.fold",
+ *     init), so K = 0 gives C = epilogue(R [+ bias]).
  *   - Staging never changes values (Tolk.Stage, module overview): the oracle
  *     has no staging at all; the GPU path's results at every stage count are
  *     graded against this one definition.
@@ -163,6 +170,9 @@ static double epilogue(int epi, double s, const float *bias, int64_t j) {
 
 typedef struct {
     int64_t M, N, K;
+    const void *R;   /* M x N residual (r_dtype, pitch ldr), or NULL */
+    int r_dtype;
+    int64_t ldr;
     const double *Ad; /* M x K decoded A, row-major, dense */
     const double *Bd; /* K x N decoded B, row-major, dense */
     int epi;
@@ -200,7 +210,9 @@ static void *gemm_rows(void *arg) {
             }
         }
         for (int64_t j = 0; j < N; ++j) {
-            const double v = epilogue(jb->epi, acc[j], jb->bias, j);
+            double s = acc[j];
+            if (jb->R) s += orc_decode(jb->r_dtype, load_bits(jb->r_dtype, jb->R, i * jb->ldr + j));
+            const double v = epilogue(jb->epi, s, jb->bias, j);
             if (jb->C_exact) jb->C_exact[i * N + j] = v;
             if (jb->S) jb->S[i * N + j] = sab[j];
             if (jb->C) store_bits(jb->out_dtype, jb->C, i * jb->ldc + j, orc_encode(jb->out_dtype, v));
@@ -227,14 +239,15 @@ static double *decode_matrix(int dtype, const void *X, int64_t rows, int64_t col
     return out;
 }
 
-/* C[i*ldc + j] = encode(out_dtype, epilogue(sum_k a_ik b_kj)) for i < M, j < N.
- * C_exact and S, when given, receive the fp64 value before rounding and the
- * sum of |a_ik b_kj| (dense M x N).  Returns 0, or -1 on a bad argument,
- * -2 when memory runs out. */
-int orc_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
-             int in_dtype, int epi, const float *bias, int out_dtype, void *C, int64_t ldc, double *C_exact,
-             double *S, int threads) {
+/* C[i*ldc + j] = encode(out_dtype, epilogue(R_ij + sum_k a_ik b_kj)) for
+ * i < M, j < N, with R_ij = 0 when R is NULL.  C_exact and S, when given,
+ * receive the fp64 value before rounding and the sum of |a_ik b_kj| (dense
+ * M x N).  Returns 0, or -1 on a bad argument, -2 when memory runs out. */
+int orc_gemm_residual(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                      const void *R, int r_dtype, int64_t ldr, int in_dtype, int epi, const float *bias,
+                      int out_dtype, void *C, int64_t ldc, double *C_exact, double *S, int threads) {
     if (M < 0 || N < 0 || K < 0) return -1;
+    if (R && (!valid_out(r_dtype) || ldr < N)) return -1;
     if (!valid_in(in_dtype) || !valid_out(out_dtype) || !valid_epi(epi)) return -1;
     if ((epi == ORC_EPI_BIAS_RELU) != (bias != NULL)) return -1;
     if (lda < K || ldb < N || ldc < N) return -1;
@@ -255,6 +268,7 @@ int orc_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     for (int t = 0; rc == 0 && t < threads; ++t) {
         gemm_job *jb = &jobs[t];
         jb->M = M; jb->N = N; jb->K = K;
+        jb->R = R; jb->r_dtype = r_dtype; jb->ldr = ldr;
         jb->Ad = Ad; jb->Bd = Bd;
         jb->epi = epi; jb->bias = bias;
         jb->out_dtype = out_dtype; jb->C = C; jb->ldc = ldc;
@@ -284,10 +298,18 @@ int orc_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     return rc;
 }
 
+int orc_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+             int in_dtype, int epi, const float *bias, int out_dtype, void *C, int64_t ldc, double *C_exact,
+             double *S, int threads) {
+    return orc_gemm_residual(M, N, K, A, lda, B, ldb, NULL, ORC_FP32, 0, in_dtype, epi, bias, out_dtype, C, ldc,
+                             C_exact, S, threads);
+}
+
 /* --------------------------------------------------- selected (i, j) only */
 
 typedef struct {
     int64_t K;
+    const void *R; int r_dtype; int64_t ldr;
     const void *A; int64_t lda;
     const void *B; int64_t ldb;
     int in_dtype, epi, out_dtype;
@@ -309,6 +331,7 @@ static void *gemm_at_range(void *arg) {
             acc += p;
             sab += fabs(p);
         }
+        if (jb->R) acc += orc_decode(jb->r_dtype, load_bits(jb->r_dtype, jb->R, i * jb->ldr + j));
         const double v = epilogue(jb->epi, acc, jb->bias, j);
         if (jb->out_exact) jb->out_exact[t] = v;
         if (jb->out_S) jb->out_S[t] = sab;
@@ -320,10 +343,12 @@ static void *gemm_at_range(void *arg) {
 /* The same definition at n chosen output positions (rows[t], cols[t]): the
  * dot product of row i of A with column j of B over ascending k.  Used where
  * the full product is too large to recompute on the host. */
-int orc_gemm_at(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
-                int in_dtype, int epi, const float *bias, int out_dtype, int64_t n, const int64_t *rows,
-                const int64_t *cols, uint32_t *out_bits, double *out_exact, double *out_S, int threads) {
+int orc_gemm_residual_at(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                         const void *R, int r_dtype, int64_t ldr, int in_dtype, int epi, const float *bias,
+                         int out_dtype, int64_t n, const int64_t *rows, const int64_t *cols, uint32_t *out_bits,
+                         double *out_exact, double *out_S, int threads) {
     if (M < 0 || N < 0 || K < 0 || n < 0) return -1;
+    if (R && (!valid_out(r_dtype) || ldr < N)) return -1;
     if (!valid_in(in_dtype) || !valid_out(out_dtype) || !valid_epi(epi)) return -1;
     if ((epi == ORC_EPI_BIAS_RELU) != (bias != NULL)) return -1;
     if (lda < K || ldb < N) return -1;
@@ -342,6 +367,7 @@ int orc_gemm_at(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, con
     for (int t = 0; t < threads; ++t) {
         at_job *jb = &jobs[t];
         jb->K = K; jb->A = A; jb->lda = lda; jb->B = B; jb->ldb = ldb;
+        jb->R = R; jb->r_dtype = r_dtype; jb->ldr = ldr;
         jb->in_dtype = in_dtype; jb->epi = epi; jb->out_dtype = out_dtype; jb->bias = bias;
         jb->rows = rows; jb->cols = cols;
         jb->out_bits = out_bits; jb->out_exact = out_exact; jb->out_S = out_S;
@@ -360,6 +386,13 @@ int orc_gemm_at(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, con
     free(jobs);
     free(tids);
     return 0;
+}
+
+int orc_gemm_at(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                int in_dtype, int epi, const float *bias, int out_dtype, int64_t n, const int64_t *rows,
+                const int64_t *cols, uint32_t *out_bits, double *out_exact, double *out_S, int threads) {
+    return orc_gemm_residual_at(M, N, K, A, lda, B, ldb, NULL, ORC_FP32, 0, in_dtype, epi, bias, out_dtype, n, rows,
+                                cols, out_bits, out_exact, out_S, threads);
 }
 
 /* Elementwise decode / encode of arrays, for the tests. */

@@ -389,3 +389,105 @@ def test_tolerance_helpers(oracle_mod):
     assert oracle_mod.ulp(np.array([65504.0]), "f16")[0] == 32.0
     t = oracle_mod.tolerance(np.array([10.0]), np.array([2.0]), "f16")
     assert t[0] == pytest.approx(1e-2 + 1e-5 + 2.0 ** -9)
+
+
+# ------------------------------------------------------------ residual
+
+def _read_residual_products():
+    cases = []
+    with open(os.path.join(GOLDEN, "residual_products.txt")) as f:
+        lines = [ln.split("#")[0].strip() for ln in f]
+    lines = [ln for ln in lines if ln]
+    i = 0
+    while i < len(lines):
+        _, name, M, N, K, epi = lines[i].split()
+        M, N, K = int(M), int(N), int(K)
+        i += 1
+        rows = lambda n: np.array([[float(t) for t in lines[i + r].split()] for r in range(n)])
+        A = rows(M); i += M
+        B = rows(K); i += K
+        bias = None if lines[i] == "-" else np.array([float(t) for t in lines[i].split()], dtype=np.float32)
+        i += 1
+        R = rows(M); i += M
+        C = rows(M); i += M
+        cases.append((name, A, B, bias, epi, R, C))
+    return cases
+
+
+def test_residual_golden(oracle_mod):
+    cases = _read_residual_products()
+    assert len(cases) == 3
+    for name, A, B, bias, epi, R, C in cases:
+        for rdt in ("f16", "f32"):
+            Rb = R.astype(np.float16).view(np.uint16) if rdt == "f16" else R.astype(np.float32).view(np.uint32)
+            Cb, exact, _ = oracle_mod.gemm(_f16(A), _f16(B), "f16", "f32", epi, bias, R_bits=Rb, r_dtype=rdt)
+            assert np.array_equal(exact, C), (name, rdt, exact)
+            assert np.array_equal(Cb, C.astype(np.float32).view(np.uint32)), name
+
+
+def test_residual_zero_is_plain_product(oracle_mod):
+    rng = np.random.default_rng(70)
+    M, N, K = 33, 21, 40
+    A = _f16(rng.normal(0, 1, (M, K)))
+    B = _f16(rng.normal(0, 1, (K, N)))
+    C0, e0, S0 = oracle_mod.gemm(A, B, "f16", "f16", "relu")
+    C1, e1, S1 = oracle_mod.gemm(A, B, "f16", "f16", "relu", R_bits=np.zeros((M, N), np.uint16), r_dtype="f16")
+    assert np.array_equal(C0, C1) and np.array_equal(e0, e1) and np.array_equal(S0, S1)
+
+
+def test_residual_adds_after_the_sum(oracle_mod):
+    """exact(A, B, R) = exact(A, B) + R, bitwise in fp64 (the fold's init is
+    added once to the finished sum), and the epilogue comes after it."""
+    rng = np.random.default_rng(71)
+    M, N, K = 29, 37, 50
+    A = _f16(rng.normal(0, 1, (M, K)))
+    B = _f16(rng.normal(0, 1, (K, N)))
+    R = rng.normal(0, 3, (M, N)).astype(np.float32)
+    _, none, S = oracle_mod.gemm(A, B, "f16", "f32")
+    _, er, Sr = oracle_mod.gemm(A, B, "f16", "f32", R_bits=R.view(np.uint32), r_dtype="f32")
+    assert np.array_equal(er, none + R.astype(np.float64)) and np.array_equal(S, Sr)
+    bias = rng.normal(0, 1, N).astype(np.float32)
+    _, ebr, _ = oracle_mod.gemm(A, B, "f16", "f32", "bias_relu", bias, R_bits=R.view(np.uint32), r_dtype="f32")
+    assert np.array_equal(ebr, np.maximum(none + R.astype(np.float64) + bias.astype(np.float64), 0.0))
+
+
+def test_residual_with_zero_operand_and_empty_k(oracle_mod):
+    rng = np.random.default_rng(72)
+    M, N = 17, 23
+    R = rng.normal(0, 10, (M, N)).astype(np.float16).view(np.uint16)
+    for K in (0, 19):
+        A = np.zeros((M, K), np.uint16)
+        B = _f16(rng.normal(0, 1, (K, N)))
+        C, exact, S = oracle_mod.gemm(A, B, "f16", "f16", R_bits=R, r_dtype="f16", K=K, N=N)
+        assert np.array_equal(C, R)                # one rounding of an fp16 value is itself
+        assert np.all(S == 0)
+
+
+def test_residual_integer_exact(oracle_mod):
+    rng = np.random.default_rng(73)
+    M, N, K = 31, 17, 384
+    Ai = rng.integers(-4, 5, (M, K))
+    Bi = rng.integers(-4, 5, (K, N))
+    Ri = rng.integers(-1000, 1001, (M, N))
+    C, exact, _ = oracle_mod.gemm(_f16(Ai), _f16(Bi), "f16", "f32", R_bits=Ri.astype(np.float32).view(np.uint32),
+                                  r_dtype="f32")
+    assert np.array_equal(exact, (Ai @ Bi + Ri).astype(np.float64))
+
+
+def test_residual_at_matches_full(oracle_mod):
+    rng = np.random.default_rng(74)
+    M, N, K = 60, 44, 70
+    A = _f16(rng.normal(0, 1, (M, K)))
+    B = _f16(rng.normal(0, 1, (K, N)))
+    R = _f16(rng.normal(0, 1, (M, N + 5)))       # padded residual rows
+    C, exact, S = oracle_mod.gemm(A, B, "f16", "bf16", "relu", R_bits=R, r_dtype="f16", N=N)
+    rows = rng.integers(0, M, 300)
+    cols = rng.integers(0, N, 300)
+    cb, ce, cs = oracle_mod.gemm_at(A, B, rows, cols, "f16", "bf16", "relu", R_bits=R, r_dtype="f16", N=N)
+    assert np.array_equal(cb, C[rows, cols]) and np.array_equal(ce, exact[rows, cols])
+
+
+def test_tolerance_added_term(oracle_mod):
+    t0 = oracle_mod.tolerance(np.array([0.0]), np.array([1.0]), "f32")
+    t1 = oracle_mod.tolerance(np.array([0.0]), np.array([1.0]), "f32", added=np.array([2.0 ** 20]))
+    assert t1[0] - t0[0] == pytest.approx(2.0 ** -3)
