@@ -43,7 +43,7 @@ import gemm_inputs  # noqa: E402
 L2_FLUSH_BYTES = 256 << 20
 METRIC = "GEMM TFLOP/s and % of GB300 dense fp16/bf16 peak (HBM GB/s for skinny-K)"
 DEFAULT_WORKLOAD = "square8192_bf16"
-HBM_BOUND = {"swin4k_proj_f16"}
+HBM_BOUND = {"swin4k_proj_f16", "swin4k_backproj_f16"}
 
 
 def parse():
@@ -163,13 +163,17 @@ class ClockSampler:
 
 
 def device_inputs(w, device):
+    """Host tensors of the workload's operands: (A, B, bias, R)."""
     import torch
-    a, b, bias = w.a_bits(), w.b_bits(), w.bias()
+    a, b, bias, r = w.a_bits(), w.b_bits(), w.bias(), w.r_bits()
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w.in_dtype]
     A = torch.from_numpy(a.view(np.int16)).view(tdt)
     B = torch.from_numpy(b.view(np.int16)).view(tdt)
     bias_t = None if bias is None else torch.from_numpy(bias.copy())
-    return A, B, bias_t
+    R = None
+    if r is not None:
+        R = torch.from_numpy(r.view(np.int32 if w.out_dtype == "f32" else np.int16)).view(out_torch_dtype(w))
+    return A, B, bias_t, R
 
 
 def out_torch_dtype(w):
@@ -197,11 +201,13 @@ def cpu_oracle_sample(w, target_s=12.0, a=None, b=None, bias=None):
     a = w.a_bits() if a is None else a
     b = w.b_bits() if b is None else b
     bias = w.bias() if bias is None else bias
+    r = w.r_bits()
     threads = os.cpu_count() or 1
     rows = min(w.M, max(threads, 16))
     while True:
         t0 = time.perf_counter()
-        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads)
+        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads,
+                    R_bits=None if r is None else r[:rows], r_dtype=w.out_dtype if r is not None else None)
         dt = time.perf_counter() - t0
         if dt >= target_s / 4 or rows >= w.M:
             break
@@ -213,14 +219,15 @@ def run_reference(args, w, rank, world):
     """The oracle arm: rank 0 only, on the host cores."""
     if rank != 0:
         return
-    a, b, bias = w.a_bits(), w.b_bits(), w.bias()
+    a, b, bias, r = w.a_bits(), w.b_bits(), w.bias(), w.r_bits()
     # size one step's sample from a calibration run
     _, rows, _, threads = cpu_oracle_sample(w, target_s=4.0, a=a, b=b, bias=bias)
     import oracle
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads)
+        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads,
+                    R_bits=None if r is None else r[:rows], r_dtype=w.out_dtype if r is not None else None)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -258,18 +265,19 @@ def config_of(w, plan):
 
 def measure(sg, w, device, stream, steps, warmup, stages, inputs=None, tune=True):
     import torch
-    A_h, B_h, bias_h = inputs if inputs is not None else device_inputs(w, device)
+    A_h, B_h, bias_h, R_h = inputs if inputs is not None else device_inputs(w, device)
     A = A_h.to(device)
     B = B_h.to(device)
     bias = None if bias_h is None else bias_h.to(device)
+    R = None if R_h is None else R_h.to(device)
     C = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), device=device)
-    if tune and stages == 0:
+    if tune and stages == 0 and R is None:
         # the library's own tuner picks the configuration (outside the timed steps)
         sg.tune(A, B, epilogue=w.epilogue, bias=bias, out=C, stream=stream)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def call():
-        sg.stage_gemm(A, B, epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream)
+        sg.stage_gemm(A, B, epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream, residual=R)
 
     def flush():
         flush_buf.fill_(1)
@@ -283,22 +291,23 @@ def measure(sg, w, device, stream, steps, warmup, stages, inputs=None, tune=True
     st = sg.device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed steps")
-    return times, (A_h, B_h, bias_h), (A, B, bias, C)
+    return times, (A_h, B_h, bias_h, R_h), (A, B, bias, C)
 
 
 def measure_e2e(sg, w, host_inputs, device, stream, steps, stages):
     """The same metric through the host-buffer API: pinned A, B (bias) copied
     in, C copied out, every step, timed with events on the stream."""
     import torch
-    A_h, B_h, bias_h = host_inputs
+    A_h, B_h, bias_h, R_h = host_inputs
     A_p = A_h.pin_memory()
     B_p = B_h.pin_memory()
     bias_p = None if bias_h is None else bias_h.pin_memory()
+    R_p = None if R_h is None else R_h.pin_memory()
     out_h = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), pin_memory=True)
 
     def call():
         sg.stage_gemm_host(A_p, B_p, out_dtype=out_h.dtype, epilogue=w.epilogue, bias_host=bias_p, stages=stages,
-                           device=device, stream=stream, out_host=out_h)
+                           device=device, stream=stream, out_host=out_h, residual_host=R_p)
 
     with torch.cuda.stream(stream):
         call()
@@ -313,6 +322,8 @@ def measure_e2e(sg, w, host_inputs, device, stream, steps, stages):
     h2d = A_p.numel() * A_p.element_size() + B_p.numel() * B_p.element_size()
     if bias_p is not None:
         h2d += bias_p.numel() * 4
+    if R_p is not None:
+        h2d += R_p.numel() * R_p.element_size()
     d2h = out_h.numel() * out_h.element_size()
     return sum(ms) / len(ms), h2d, d2h
 
@@ -391,7 +402,7 @@ def main():
     ms = sum_ms / len(times)
     value = whole_job_tflops(w.flops, world, len(times), sum_ms)
     plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages)
-    plan["tuned"] = (not args.no_tune) and args.stages == 0
+    plan["tuned"] = (not args.no_tune) and args.stages == 0 and w.dist_r is None
 
     e2e = None
     if not args.no_e2e:
@@ -419,7 +430,7 @@ def main():
 
     if rank == 0 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD:
         sec = []
-        for name in ("relu4096_f16", "swin4k_proj_f16"):
+        for name in ("relu4096_f16", "swin4k_proj_f16", "swin4k_backproj_f16"):
             ws = gemm_inputs.WORKLOADS[name]
             t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=not args.no_tune)
             del dt

@@ -17,7 +17,8 @@ Generator (counter-based, so any element can be drawn independently):
     storage type: fp16 directly; bf16 through binary32 (float64 -> float32
     RNE, then float32 -> bf16 RNE on the bit pattern); fp32 bias directly.
 
-Streams: A = 0, B = 1, bias = 2.  Workload w (1..5) uses seed 1000 + w.
+Streams: A = 0, B = 1, bias = 2, residual = 3.  Workload w (1..6) uses seed
+1000 + w.
 """
 from __future__ import annotations
 
@@ -30,7 +31,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 22
 
-STREAM_A, STREAM_B, STREAM_BIAS = 0, 1, 2
+STREAM_A, STREAM_B, STREAM_BIAS, STREAM_RESIDUAL = 0, 1, 2, 3
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -129,6 +130,7 @@ class Workload:
     dist_bias: tuple | None
     seed: int
     description: str
+    dist_r: tuple | None = None   # residual R (M x N, output type), if the workload has one
 
     @property
     def flops(self) -> int:
@@ -141,6 +143,8 @@ class Workload:
         b = 2 * self.M * self.K + 2 * self.K * self.N + out_size * self.M * self.N
         if self.epilogue == "bias_relu":
             b += 4 * self.N
+        if self.dist_r is not None:
+            b += out_size * self.M * self.N
         return b
 
     def a_bits(self, ld: int | None = None) -> np.ndarray:
@@ -148,6 +152,13 @@ class Workload:
 
     def b_bits(self, ld: int | None = None) -> np.ndarray:
         return matrix_bits(self.seed, STREAM_B, self.K, self.N, self.dist_b, self.in_dtype, ld)
+
+    def r_bits(self) -> np.ndarray | None:
+        """The residual's bit patterns (M x N, the output's storage type)."""
+        if self.dist_r is None:
+            return None
+        return to_storage_bits(draw(self.seed, STREAM_RESIDUAL, self.M * self.N, self.dist_r),
+                               self.out_dtype).reshape(self.M, self.N)
 
     def bias(self) -> np.ndarray | None:
         if self.dist_bias is None:
@@ -177,6 +188,12 @@ WORKLOADS = {
         ("normal", 0.0, 1.0), ("normal", 0.0, 0.1), ("normal", 0.0, 0.1), 1005,
         "skinny-K token projection, 3840x2160 frame in 4x4 patches: M=518400 tokens, K=96 -> N=384, "
         "C = relu(A.W + b), fp16 in/out, fp32 bias"),
+    "swin4k_backproj_f16": Workload(
+        "swin4k_backproj_f16", 518400, 96, 384, "f16", "f16", "none",
+        ("normal", 0.0, 1.0), ("normal", 0.0, 0.05), None, 1006,
+        "skinny-N back-projection of the Swin MLP band on a 3840x2160 frame in 4x4 patches: M=518400 tokens, "
+        "K=384 -> N=96, C = A.W + R with the residual R as the accumulator's seed, fp16 in/out",
+        dist_r=("normal", 0.0, 1.0)),
 }
 
 # The five workloads in the order they are listed for this path.

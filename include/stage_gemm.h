@@ -122,6 +122,29 @@ int sg_gemm(int64_t M, int64_t N, int64_t K,
             int in_dtype, int out_dtype, int epilogue,
             const float* bias, int stages, void* stream);
 
+/*
+ * sg_gemm_residual -- C = epilogue(A . B + R): the residual R (M x N,
+ * row-major, pitch ldr >= N, of type out_dtype) is added to the fp32
+ * accumulator before the bias and the ReLU, the fold starting from R
+ * instead of zeros.  This is the back-projection of the Swin-layer MLP band
+ * (d4r, rrswin_enc2_epilogues.md, "Shape of the whole MLP band": its MMA
+ * takes the previous accumulator as its C input) and gizml:tile's
+ * "Program.fold" with a non-zero init; K = 0 gives C = epilogue(R [+bias]).
+ * R may be C itself (same pointer and ldr == ldc): every element is read
+ * before it is written.  Any other overlap of R and C is SG_ERR_ALIAS; R
+ * not aligned to its elements is SG_ERR_ALIGN; a NULL R is SG_ERR_ARG.  An
+ * R whose base is 16-byte aligned and whose pitch is a multiple of 16 bytes
+ * is loaded by TMA, any other by element loads.  Everything else is as for
+ * sg_gemm.
+ */
+int sg_gemm_residual(int64_t M, int64_t N, int64_t K,
+                     const void* A, int64_t lda,
+                     const void* B, int64_t ldb,
+                     const void* R, int64_t ldr,
+                     void* C, int64_t ldc,
+                     int in_dtype, int out_dtype, int epilogue,
+                     const float* bias, int stages, void* stream);
+
 /* The launch configuration sg_gemm would use for TMA-legal A and B (no GPU
  * work is queued).  Needs a current CUDA device; returns the same codes as
  * sg_gemm. */

@@ -68,6 +68,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         lib.sg_gemm.restype = i32
         lib.sg_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
+        lib.sg_gemm_residual.restype = i32
+        lib.sg_gemm_residual.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
         lib.sg_plan.restype = i32
         lib.sg_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i64, vp, ctypes.POINTER(PlanInfo)]
         lib.sg_device_status.restype = i32
@@ -142,14 +144,17 @@ def gemm_raw(M: int, N: int, K: int, A_ptr: int, lda: int, B_ptr: int, ldb: int,
                                   bias_ptr, stages, stream_ptr)
 
 
-def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: int = 0, out=None, stream=None):
-    """C = epilogue(A @ B) on A's CUDA device, queued on ``stream`` (default:
-    the current stream).  A (M x K) and B (K x N) are row-major fp16 or bf16
-    CUDA tensors of one dtype; ``out_dtype`` is float32 (default), float16
-    or bfloat16; ``bias`` is an fp32 CUDA vector of N values for
-    ``epilogue="bias_relu"``; ``stages`` is the operand ring depth (0: the
-    largest that fits).  ``out`` may be a preallocated row-major M x N view
-    (its padding columns are never written)."""
+def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: int = 0, out=None, stream=None,
+               residual=None):
+    """C = epilogue(A @ B [+ residual]) on A's CUDA device, queued on
+    ``stream`` (default: the current stream).  A (M x K) and B (K x N) are
+    row-major fp16 or bf16 CUDA tensors of one dtype; ``out_dtype`` is
+    float32 (default), float16 or bfloat16; ``bias`` is an fp32 CUDA vector
+    of N values for ``epilogue="bias_relu"``; ``residual`` is an M x N
+    row-major tensor of the output dtype added to the accumulator before the
+    bias and the ReLU (it may be ``out`` itself); ``stages`` is the operand
+    ring depth (0: the largest that fits).  ``out`` may be a preallocated
+    row-major M x N view (its padding columns are never written)."""
     torch = _torch()
     if A.device.type != "cuda" or B.device.type != "cuda":
         raise ValueError("A and B must be CUDA tensors")
@@ -172,18 +177,26 @@ def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: 
         if bias.dtype != torch.float32 or bias.device != A.device or bias.numel() != N or not bias.is_contiguous():
             raise ValueError("bias must be a contiguous fp32 CUDA vector of N values")
         bptr = bias.data_ptr()
-    rc = gemm_raw(M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), out.data_ptr(),
-                  _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype), EPILOGUES[epilogue], bptr,
-                  int(stages), _stream_ptr(stream, A.device).value)
+    if residual is not None:
+        if residual.dtype != out.dtype or tuple(residual.shape) != (M, N) or residual.device != A.device:
+            raise ValueError("residual must be an M x N CUDA tensor of the output dtype")
+        rc = load_library().sg_gemm_residual(
+            M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), residual.data_ptr(),
+            _row_pitch(residual), out.data_ptr(), _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype),
+            EPILOGUES[epilogue], bptr, int(stages), _stream_ptr(stream, A.device).value)
+    else:
+        rc = gemm_raw(M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), out.data_ptr(),
+                      _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype), EPILOGUES[epilogue], bptr,
+                      int(stages), _stream_ptr(stream, A.device).value)
     _check(rc)
     return out
 
 
 def stage_gemm_host(A_host, B_host, out_dtype=None, epilogue: str = "none", bias_host=None, stages: int = 0,
-                    device=None, stream=None, out_host=None):
-    """End-to-end call on host tensors: copies A, B (and bias) to the device,
-    runs ``stage_gemm`` and copies C back into ``out_host`` (pinned host
-    memory is used for asynchronous copies).  Returns the host tensor."""
+                    device=None, stream=None, out_host=None, residual_host=None):
+    """End-to-end call on host tensors: copies A, B (bias, residual) to the
+    device, runs ``stage_gemm`` and copies C back into ``out_host`` (pinned
+    host memory is used for asynchronous copies).  Returns the host tensor."""
     torch = _torch()
     dev = torch.device(device or "cuda")
     s = stream if stream is not None else torch.cuda.current_stream(dev)
@@ -191,7 +204,8 @@ def stage_gemm_host(A_host, B_host, out_dtype=None, epilogue: str = "none", bias
         A = A_host.to(dev, non_blocking=True)
         B = B_host.to(dev, non_blocking=True)
         bias = None if bias_host is None else bias_host.to(dev, non_blocking=True)
-        C = stage_gemm(A, B, out_dtype=out_dtype, epilogue=epilogue, bias=bias, stages=stages, stream=s)
+        R = None if residual_host is None else residual_host.to(dev, non_blocking=True)
+        C = stage_gemm(A, B, out_dtype=out_dtype, epilogue=epilogue, bias=bias, stages=stages, stream=s, residual=R)
         if out_host is None:
             out_host = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
         out_host.copy_(C, non_blocking=True)

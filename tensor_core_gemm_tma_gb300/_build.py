@@ -1,7 +1,8 @@
 """Builds the in-tree CUDA library libstage_gemm.so for sm_103a with nvcc.
 
-One translation unit, one -gencode; the result sits next to this file so the
-binding loads it from the source tree."""
+The host API unit and the kernel-instantiation units (sg_inst_*.cu) are
+compiled in parallel (one -gencode), then linked into one shared library
+that sits next to this file, so the binding loads it from the source tree."""
 from __future__ import annotations
 
 import glob
@@ -15,6 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libstage_gemm.so")
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+COMMON = ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC"]
 
 
 def _nvcc() -> str:
@@ -24,9 +26,12 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libstage_gemm.so")
 
 
+def _units():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
-                  glob.glob(os.path.join(INCLUDE, "*.h")))
+    return sorted(_units() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def needs_build() -> bool:
@@ -39,15 +44,34 @@ def needs_build() -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not needs_build():
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *ARCH_FLAGS, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I", INCLUDE, os.path.join(CSRC, "sg_api.cu"), "-o", tmp]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({res.returncode}):\n{' '.join(cmd)}\n{res.stdout}\n{res.stderr}")
-    if verbose and (res.stdout or res.stderr):
-        print(res.stdout + res.stderr)
-    os.replace(tmp, LIB)
+    nvcc = _nvcc()
+    tag = f".tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in _units():
+        obj = os.path.join(CSRC, os.path.basename(src)[:-3] + tag + ".o")
+        cmd = [nvcc, *ARCH_FLAGS, *COMMON, "-I", INCLUDE, "-c", src, "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        objs.append(obj)
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
+    failed = []
+    for cmd, p in procs:
+        out, _ = p.communicate()
+        if p.returncode != 0:
+            failed.append(f"{' '.join(cmd)}\n{out}")
+        elif verbose and out:
+            print(out)
+    try:
+        if failed:
+            raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
+        tmp = LIB + tag
+        link = [nvcc, *ARCH_FLAGS, "-shared", *objs, "-o", tmp]
+        res = subprocess.run(link, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"link failed:\n{' '.join(link)}\n{res.stdout}\n{res.stderr}")
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB

@@ -18,7 +18,7 @@
 #include <tuple>
 #include <vector>
 
-#include "sg_kernel.cuh"
+#include "sg_launch.cuh"
 #include "stage_gemm.h"
 
 namespace {
@@ -40,8 +40,9 @@ struct DevState {
     int smem_per_sm = 0;
     int major = 0, minor = 0;
     int* status = nullptr;  // device status word (4 bytes, library-owned)
-    bool attr_done[3][3][3] = {};    // [tile-width variant][output type][mode - 1]
-    int max_clusters[3][3][3] = {};  // co-resident clusters of each instantiation (0: not queried)
+    // per kernel instantiation [tile width][output type][mode - 1][residual]:
+    bool attr_done[3][3][3][2] = {};    // dynamic shared-memory attribute set
+    int max_clusters[3][3][3][2] = {};  // co-resident clusters (0: not queried)
 };
 
 std::mutex g_mu;
@@ -299,77 +300,33 @@ int encode_2d(CUtensorMap* tm, int dt, const void* ptr, int64_t inner, int64_t o
     return r == CUDA_SUCCESS ? SG_OK : SG_ERR_CUDA;
 }
 
-template <int BN, int OUT, int MODE>
-int launch_t(DevState& st, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-             const sg::Params& prm, cudaStream_t stream) {
-    constexpr int CM = MODE == 1 ? 1 : 2;
-    auto kern = sg::sg_gemm_kernel<BN, OUT, MODE>;
-    const int bi = BN == 128 ? 0 : BN == 192 ? 1 : 2;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CM;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(sg::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int grid = pl.grid;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!st.attr_done[bi][OUT][MODE - 1]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, st.smem_optin) !=
-                cudaSuccess)
-                return SG_ERR_CUDA;
-            st.attr_done[bi][OUT][MODE - 1] = true;
-        }
-        if (CM > 1) {
-            int& mc = st.max_clusters[bi][OUT][MODE - 1];
-            if (mc == 0) {
-                cfg.gridDim = dim3(static_cast<unsigned>(pl.grid), 1, 1);
-                int n = 0;
-                mc = (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) ? n : -1;
-                cudaGetLastError();  // a failed query is not a launch error
-            }
-            // a persistent grid larger than what can be co-resident only adds a tail
-            if (mc > 0 && grid > mc * CM) grid = mc * CM;
-        }
-    }
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm) != cudaSuccess) {
-        cudaGetLastError();
-        return SG_ERR_CUDA;
-    }
-    return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
-}
-
-template <int BN, int MODE>
-int launch_bn(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
-              const CUtensorMap& tc, const sg::Params& prm, cudaStream_t stream) {
-    switch (out_dtype) {
-        case SG_F32: return launch_t<BN, SG_F32, MODE>(st, pl, ta, tb, tc, prm, stream);
-        case SG_F16: return launch_t<BN, SG_F16, MODE>(st, pl, ta, tb, tc, prm, stream);
-        default: return launch_t<BN, SG_BF16, MODE>(st, pl, ta, tb, tc, prm, stream);
-    }
-}
-
+// Launch the instantiation the plan names (it lives in one of the
+// sg_inst_*.cu units).
 int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
-                const CUtensorMap& tc, const sg::Params& prm, cudaStream_t stream) {
-    if (pl.mode == 3) {
-        if (pl.bn == 256) return launch_bn<256, 3>(st, out_dtype, pl, ta, tb, tc, prm, stream);
-        return launch_bn<128, 3>(st, out_dtype, pl, ta, tb, tc, prm, stream);
-    }
-    if (pl.mode == 2) {
-        if (pl.bn == 256) return launch_bn<256, 2>(st, out_dtype, pl, ta, tb, tc, prm, stream);
-        return launch_bn<128, 2>(st, out_dtype, pl, ta, tb, tc, prm, stream);
-    }
-    switch (pl.bn) {
-        case 256: return launch_bn<256, 1>(st, out_dtype, pl, ta, tb, tc, prm, stream);
-        case 192: return launch_bn<192, 1>(st, out_dtype, pl, ta, tb, tc, prm, stream);
-        default: return launch_bn<128, 1>(st, out_dtype, pl, ta, tb, tc, prm, stream);
-    }
+                const CUtensorMap& tc, const CUtensorMap& tr, const sg::Params& prm, bool residual,
+                cudaStream_t stream) {
+    sg::LaunchFn fn = nullptr;
+    if (pl.mode == 1)
+        fn = residual ? sg::launcher_res_single(pl.bn, out_dtype) : sg::launcher_plain_single(pl.bn, out_dtype);
+    else
+        fn = residual ? sg::launcher_res_pair(pl.bn, out_dtype, pl.mode)
+                      : sg::launcher_plain_pair(pl.bn, out_dtype, pl.mode);
+    if (!fn) return SG_ERR_ARG;
+    const int bi = pl.bn == 128 ? 0 : pl.bn == 192 ? 1 : 2;
+    sg::LaunchArgs a;
+    a.ta = &ta;
+    a.tb = &tb;
+    a.tc = &tc;
+    a.tr = &tr;
+    a.prm = &prm;
+    a.grid = pl.grid;
+    a.smem = pl.smem;
+    a.smem_optin = st.smem_optin;
+    a.stream = stream;
+    a.mu = &g_mu;
+    a.attr_done = &st.attr_done[bi][out_dtype][pl.mode - 1][residual ? 1 : 0];
+    a.max_clusters = &st.max_clusters[bi][out_dtype][pl.mode - 1][residual ? 1 : 0];
+    return fn(a) == 0 ? SG_OK : SG_ERR_CUDA;
 }
 
 // Plan, build the tensor maps and kernel parameters, and launch (shared by
@@ -415,7 +372,7 @@ bool lookup_tuned(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, 
 int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
                     int stages, int64_t skip_load, cudaStream_t stream, const Choice* forced = nullptr,
-                    Plan* used = nullptr) {
+                    Plan* used = nullptr, const void* R = nullptr, int64_t ldr = 0) {
     const bool a_tma = tma_legal(A, M, lda);
     const bool b_tma = tma_legal(B, K, ldb);
     Choice tuned;
@@ -428,18 +385,22 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     if (rc != SG_OK) return rc;
     if (used) *used = pl;
 
-    alignas(64) CUtensorMap ta, tb, tc;
+    alignas(64) CUtensorMap ta, tb, tc, tr;
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     std::memset(&tc, 0, sizeof(tc));
+    std::memset(&tr, 0, sizeof(tr));
     if (K > 0) {
         if (a_tma && (rc = encode_2d(&ta, in_dtype, A, K, M, lda * 2, sg::BK, sg::BM)) != SG_OK) return rc;
         if (b_tma && (rc = encode_2d(&tb, in_dtype, B, N, K, ldb * 2, 64, sg::BK)) != SG_OK) return rc;
     }
+    const int oes = elem_bytes(out_dtype);
     if (pl.tma_store) {
-        const int oes = elem_bytes(out_dtype);
         if ((rc = encode_2d(&tc, out_dtype, C, N, M, ldc * oes, 128 / oes, 32)) != SG_OK) return rc;
     }
+    // a residual box has the shape of an output box (32 rows x 128 bytes)
+    const bool r_tma = R != nullptr && c_tma_legal(R, M, ldr, out_dtype);
+    if (r_tma && (rc = encode_2d(&tr, out_dtype, R, N, M, ldr * oes, 128 / oes, 32)) != SG_OK) return rc;
 
     sg::Params prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -467,7 +428,10 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.B = static_cast<const uint16_t*>(B);
     prm.lda = lda;
     prm.ldb = ldb;
-    return launch_plan(st, out_dtype, pl, ta, tb, tc, prm, stream);
+    prm.R = R;
+    prm.ldr = ldr;
+    prm.r_tma = r_tma ? 1 : 0;
+    return launch_plan(st, out_dtype, pl, ta, tb, tc, tr, prm, R != nullptr, stream);
 }
 
 }  // namespace
@@ -483,6 +447,25 @@ int sg_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
     if ((rc = device_state(&st)) != SG_OK) return rc;
     return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
                            g_skip_load.load(), static_cast<cudaStream_t>(stream));
+}
+
+int sg_gemm_residual(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                     const void* R, int64_t ldr, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue,
+                     const float* bias, int stages, void* stream) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    if (!R || ldr < N || ldr > 0x7FFFFFFF) return SG_ERR_ARG;
+    const int oes = elem_bytes(out_dtype);
+    if (reinterpret_cast<uintptr_t>(R) % oes) return SG_ERR_ALIGN;
+    // R may be C itself (each element is read before it is written); any
+    // other overlap of the two would race
+    const bool same = (R == C && ldr == ldc);
+    if (!same && overlap(C, span_bytes(M, N, ldc, oes), R, span_bytes(M, N, ldr, oes))) return SG_ERR_ALIAS;
+    DevState* st = nullptr;
+    if ((rc = device_state(&st)) != SG_OK) return rc;
+    return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                           g_skip_load.load(), static_cast<cudaStream_t>(stream), nullptr, nullptr, R, ldr);
 }
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages, int64_t ldc,

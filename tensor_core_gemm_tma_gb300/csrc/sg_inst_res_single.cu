@@ -1,0 +1,21 @@
+// sg_inst_res_single.cu -- kernel instantiations: with a residual, single-CTA mode.
+#include "sg_launch.cuh"
+
+namespace sg {
+
+LaunchFn launcher_res_single(int bn, int out) {
+    switch (bn * 4 + out) {
+        case 128 * 4 + SG_F32: return &launch_kernel<128, SG_F32, 1, true>;
+        case 128 * 4 + SG_F16: return &launch_kernel<128, SG_F16, 1, true>;
+        case 128 * 4 + SG_BF16: return &launch_kernel<128, SG_BF16, 1, true>;
+        case 192 * 4 + SG_F32: return &launch_kernel<192, SG_F32, 1, true>;
+        case 192 * 4 + SG_F16: return &launch_kernel<192, SG_F16, 1, true>;
+        case 192 * 4 + SG_BF16: return &launch_kernel<192, SG_BF16, 1, true>;
+        case 256 * 4 + SG_F32: return &launch_kernel<256, SG_F32, 1, true>;
+        case 256 * 4 + SG_F16: return &launch_kernel<256, SG_F16, 1, true>;
+        case 256 * 4 + SG_BF16: return &launch_kernel<256, SG_BF16, 1, true>;
+        default: return nullptr;
+    }
+}
+
+}  // namespace sg

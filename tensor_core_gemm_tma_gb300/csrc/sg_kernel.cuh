@@ -79,11 +79,12 @@ constexpr int EPI_BUF_BYTES = 32 * 128;     // one warp's staging buffer: 32 row
 constexpr int TMEM_COLS = 512;              // the whole tensor memory of the SM
 constexpr int MAX_ACC = 4;                  // accumulators in flight (512 / 128)
 constexpr int SMEM_ALIGN = 1024;            // 128-byte swizzle atoms repeat every 1024 bytes
-constexpr int BAR_AREA = 256;
+constexpr int BAR_AREA = 512;
 
 // Device status word values: 0 = fine; otherwise a timeout site code.
 constexpr int STATUS_TIMEOUT = 0x5400;
-constexpr int SITE_PRODUCER_EMPTY = 1, SITE_MMA_TMEM_EMPTY = 2, SITE_MMA_FULL = 3, SITE_EPI_TMEM_FULL = 4;
+constexpr int SITE_PRODUCER_EMPTY = 1, SITE_MMA_TMEM_EMPTY = 2, SITE_MMA_FULL = 3, SITE_EPI_TMEM_FULL = 4,
+              SITE_EPI_RESIDUAL = 5;
 
 // BN: accumulator columns per tile; BL: B columns this CTA stages per K chunk
 // (BN, or BN / 2 for the paired MMA).
@@ -123,6 +124,11 @@ struct Params {
     const uint16_t* A;     // 16-bit elements; used when a_tma == 0
     const uint16_t* B;     // used when b_tma == 0
     int64_t lda, ldb;
+    // Residual R (M x N, the output's type), added to the accumulator before
+    // the bias and the ReLU; may be C itself (same address and pitch).
+    const void* R;
+    int64_t ldr;
+    int32_t r_tma;         // 1: R tiles are loaded by TMA, 0: by element loads
 };
 
 // Element-load staging of one A chunk (rows m0.., k0..k0+63) into the same
@@ -192,7 +198,7 @@ __device__ __forceinline__ void tile_coords(int tile, const Params& p, uint32_t 
 
 // Wait for phase `parity` of `bar`, giving up after `limit` ns or when another
 // role has aborted.  A give-up by this wait records `site` in the status word.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
                                           uint64_t limit, int site) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -212,7 +218,7 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
 
 // Bounded wait that ignores the abort flag: used to drain a role's own
 // asynchronous work before the CTA exits.
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
+static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -242,6 +248,52 @@ __device__ __forceinline__ uint32_t pack2_relu(float lo, float hi) {
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int OUT>
+__device__ __forceinline__ float load_one(const void* X, int64_t idx) {
+    if constexpr (OUT == SG_F32) {
+        return __ldg(static_cast<const float*>(X) + idx);
+    } else if constexpr (OUT == SG_F16) {
+        return __half2float(__ldg(static_cast<const __half*>(X) + idx));
+    } else {
+        return __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(X) + idx));
+    }
+}
+
+// Adds this lane's row of a residual tile that TMA placed, 128-byte
+// swizzled, in the staging buffer (row `lane` at lane * 128, 16-byte chunk j
+// at j ^ (lane mod 8)) -- the same layout the store path writes.
+template <int OUT, int COLS>
+__device__ __forceinline__ void add_staged_residual(float (&v)[COLS], uint32_t rowaddr, int lane) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(rowaddr + ((j ^ (lane & 7)) << 4))
+                     : "memory");
+        if constexpr (OUT == SG_F32) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) v[4 * j + t] += __uint_as_float(w[t]);
+        } else {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                float lo, hi;
+                if constexpr (OUT == SG_F16) {
+                    const __half2 h = *reinterpret_cast<const __half2*>(&w[t]);
+                    lo = __low2float(h);
+                    hi = __high2float(h);
+                } else {
+                    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[t]);
+                    lo = __low2float(h);
+                    hi = __high2float(h);
+                }
+                v[8 * j + 2 * t] += lo;
+                v[8 * j + 2 * t + 1] += hi;
+            }
+        }
+    }
 }
 
 template <int OUT>
@@ -277,10 +329,13 @@ __device__ __forceinline__ void add_bias(float (&v)[COLS], const float* __restri
     }
 }
 
-template <int BN, int OUT, int MODE>
+// RES: the kernel adds a residual R (C = epilogue(A . B + R)); a separate
+// instantiation, so the plain epilogue carries none of its work.
+template <int BN, int OUT, int MODE, bool RES>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const Params p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
+                   const Params p) {
     static_assert(MODE >= 1 && MODE <= 3, "mode 1, 2 or 3");
     constexpr int CM = (MODE == 1) ? 1 : 2;    // CTAs per cluster
     constexpr bool PAIR = (MODE == 3);         // paired MMA (cta_group::2)
@@ -303,7 +358,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int stages = p.stages;
 
     const uint32_t bar0 = base + L::bar_offset(stages);
-    // barrier slots: full[0..7], empty[8..15], tmem_full[16..19], tmem_empty[20..23], drain[24]
+    // barrier slots: full[0..7], empty[8..15], tmem_full[16..19], tmem_empty[20..23], drain[24],
+    // then the tensor-memory address and abort flag, then residual[0..7] at 32..39
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (SG_MAX_STAGES + s); };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + b); };
@@ -312,6 +368,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t* tmem_slot =
         reinterpret_cast<uint32_t*>(gbase + L::bar_offset(stages) + 8 * (2 * SG_MAX_STAGES + 2 * MAX_ACC + 1));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    auto rres_bar = [&](int e) { return bar0 + 8u * (32 + e); };  // residual tile landed (one per epilogue warp)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -326,6 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(tempty_bar(b), PAIR ? 2 * EPI_WARPS : EPI_WARPS);  // paired: both CTAs' epilogues
         }
         mbar_init(drain_bar, 1);
+        for (int e = 0; e < EPI_WARPS; ++e) mbar_init(rres_bar(e), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -335,6 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (p.b_tma) prefetch_tmap(&tmB);
         }
         if (p.tma_store) prefetch_tmap(&tmC);
+        if (RES && p.r_tma) prefetch_tmap(&tmR);
     }
     __syncwarp();  // reconverge before the warp-collective (.sync.aligned) instructions below
     if (warp == 1) {
@@ -539,18 +598,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int SPLIT = EPI_WARPS / 4;      // warps sharing a quarter
         const int part = e / 4;                   // which of them: takes column chunks part, part+SPLIT, ...
         const uint32_t buf = base + L::epi_offset(stages) + e * EPI_BUF_BYTES;
+        const bool r_staged = RES && p.r_tma;  // residual tiles arrive by TMA in the staging buffer
+        uint32_t r_phase = 0;
+        bool r_pending = false;                    // a residual load is in flight into `buf`
+        // Starts the TMA load of the residual box this warp needs for output
+        // columns col0.. (after the previous store has read the buffer).
+        auto load_residual = [&](int row0, int col0) {
+            if (lane == 0) {
+                bulk_wait_group_read<0>();
+                mbar_arrive_expect_tx(rres_bar(e), EPI_BUF_BYTES);
+                tma_load_2d(buf, &tmR, rres_bar(e), col0, row0);
+            }
+            r_pending = true;
+        };
         uint32_t ab = 0, aph = 0;
         for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
             int mb, nb;
             tile_coords<CM>(tile, p, rank, mb, nb);
+            const int row0 = mb * BM + q * 32;
+            const int row = row0 + lane;
+            // the residual of this warp's first chunk loads while the MMAs run
+            if (r_staged && row0 < p.M && nb * BN + part * COLS < p.N) load_residual(row0, nb * BN + part * COLS);
             if (p.k_chunks > 0) {
                 const bool w = wait_bounded(tfull_bar(ab), aph, abort_flag, p.status, p.wait_limit_ns,
                                             SITE_EPI_TMEM_FULL);
                 if (!__all_sync(0xffffffffu, w)) break;
                 tc_fence_after();
             }
-            const int row0 = mb * BM + q * 32;
-            const int row = row0 + lane;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN;
 #pragma unroll 1
             for (int c = part * COLS; c < BN; c += SPLIT * COLS) {
@@ -575,6 +649,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < COLS; ++i) v[i] = 0.0f;
                 }
+                if constexpr (RES) {
+                    if (r_staged) {
+                        if (row0 < p.M && col0 < p.N) {  // warp-uniform: a residual box was loaded
+                            const bool w = wait_bounded(rres_bar(e), r_phase, abort_flag, p.status, p.wait_limit_ns,
+                                                        SITE_EPI_RESIDUAL);
+                            if (!__all_sync(0xffffffffu, w)) break;
+                            r_phase ^= 1u;
+                            r_pending = false;
+                            add_staged_residual<OUT, COLS>(v, buf + lane * 128, lane);
+                        }
+                    } else if (row < p.M) {
+#pragma unroll
+                        for (int i = 0; i < COLS; ++i) {
+                            const int col = col0 + i;
+                            if (col < p.N) v[i] += load_one<OUT>(p.R, static_cast<int64_t>(row) * p.ldr + col);
+                        }
+                    }
+                }
                 if (p.epi == SG_EPI_BIAS_RELU) add_bias<COLS>(v, p.bias, col0, p.N);
                 const bool relu = p.epi != SG_EPI_NONE;
                 if (OUT == SG_F32 || !p.tma_store) {
@@ -585,7 +677,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (p.tma_store) {
                     if (row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
-                        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
+                        // the previous store has read the buffer (a staged residual already waited)
+                        if (lane == 0 && !r_staged) bulk_wait_group_read<0>();
                         __syncwarp();
                         const uint32_t rowaddr = buf + lane * 128;
 #pragma unroll
@@ -625,6 +718,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 __syncwarp();  // the next tcgen05.ld is warp-collective
+                // the next chunk's residual (the store just issued must read the buffer first)
+                const int cn = c + SPLIT * COLS;
+                if (r_staged && cn < BN && row0 < p.M && nb * BN + cn < p.N) load_residual(row0, nb * BN + cn);
             }
             if (p.k_chunks > 0) {
                 tc_fence_before();
@@ -642,6 +738,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 aph ^= 1u;
             }
         }
+        // leaving early with a residual load in flight: let it land first
+        if (r_pending && lane == 0) wait_drain(rres_bar(e), r_phase, p.wait_limit_ns);
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
     }
