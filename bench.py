@@ -57,8 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg (profiling runs)")
     ap.add_argument("--no-secondary", action="store_true", help="skip the other-workload summary")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
-    ap.add_argument("--no-tune", action="store_true",
-                    help="use the planner's heuristic instead of tuning the configuration first (sg_tune)")
+    ap.add_argument("--tune", action="store_true",
+                    help="tune the launch configuration first (sg_tune) instead of the planner's heuristic")
     return ap.parse_args()
 
 
@@ -396,13 +396,13 @@ def main():
     with clocks:
         barrier()
         times, host_inputs, dev_tensors = measure(sg, w, device, stream, args.steps, args.warmup, args.stages,
-                                                  inputs=host_inputs, tune=not args.no_tune)
+                                                  inputs=host_inputs, tune=args.tune)
         barrier()
     sum_ms = max_over_ranks(sum(times), pg, device)
     ms = sum_ms / len(times)
     value = whole_job_tflops(w.flops, world, len(times), sum_ms)
     plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages)
-    plan["tuned"] = (not args.no_tune) and args.stages == 0 and w.dist_r is None
+    plan["tuned"] = args.tune and args.stages == 0 and w.dist_r is None
 
     e2e = None
     if not args.no_e2e:
@@ -432,7 +432,7 @@ def main():
         sec = []
         for name in ("relu4096_f16", "swin4k_proj_f16", "swin4k_backproj_f16"):
             ws = gemm_inputs.WORKLOADS[name]
-            t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=not args.no_tune)
+            t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=args.tune)
             del dt
             m2 = sum(t2) / len(t2)
             sec.append({"workload": name, "ms_per_step": m2, "TFLOP/s": ws.flops / (m2 * 1e-3) / 1e12,
