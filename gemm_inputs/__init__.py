@@ -86,11 +86,29 @@ def draw(seed: int, stream: int, n: int, dist: tuple) -> np.ndarray:
 
 def to_storage_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     """float64 -> bit patterns of the storage type (uint16 for fp16/bf16,
-    uint32 for fp32), round to nearest even."""
+    uint32 for fp32, uint8 for e4m3), round to nearest even (e4m3 saturates
+    at +-448 first)."""
     if dtype == "f16":
         return x.astype(np.float16).view(np.uint16)
     if dtype == "f32":
         return x.astype(np.float32).view(np.uint32)
+    if dtype == "e4m3":
+        # OCP FP8 E4M3: saturate to the largest finite value (+-448), then
+        # round to nearest even on the 3-bit fraction (quantum 2^(e-3) for
+        # |x| in [2^e, 2^(e+1)), 2^-9 below the smallest normal 2^-6)
+        a = np.minimum(np.abs(x), 448.0)
+        sign = np.signbit(x).astype(np.uint8) << np.uint8(7)
+        _, ex = np.frexp(a)                    # a = m * 2^ex, m in [0.5, 1)
+        e = np.maximum(ex - 1, -6)             # exponent of the binade (clamped to the subnormal range)
+        q = np.ldexp(1.0, (e - 3).astype(np.int64))
+        m = np.rint(a / q)                     # np.rint rounds half to even
+        carry = m >= 16.0
+        e = np.where(carry, e + 1, e)
+        m = np.where(carry, 8.0, m)
+        normal = m >= 8.0
+        enc = np.where(normal, ((e + 7).astype(np.int64) << 3) | (m.astype(np.int64) - 8), m.astype(np.int64))
+        enc = np.where(a == 0, 0, enc)
+        return (enc.astype(np.uint8) | sign).astype(np.uint8)
     if dtype == "bf16":
         f = x.astype(np.float32).view(np.uint32)
         nan = (f & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
@@ -104,8 +122,9 @@ def to_storage_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 def matrix_bits(seed: int, stream: int, rows: int, cols: int, dist: tuple, dtype: str,
                 ld: int | None = None) -> np.ndarray:
-    """A rows x ld uint16 bit matrix whose first ``cols`` columns hold the
-    seeded values (row-major draw order); padding columns are zero."""
+    """A rows x ld bit matrix (uint16, or uint8 for e4m3) whose first
+    ``cols`` columns hold the seeded values (row-major draw order); padding
+    columns are zero."""
     ld = cols if ld is None else ld
     vals = to_storage_bits(draw(seed, stream, rows * cols, dist), dtype).reshape(rows, cols)
     if ld == cols:

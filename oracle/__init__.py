@@ -34,9 +34,9 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 # The oracle's own type codes (must match the #defines in oracle.c only).
-_DT = {"f32": ord("S"), "f16": ord("H"), "bf16": ord("B")}
+_DT = {"f32": ord("S"), "f16": ord("H"), "bf16": ord("B"), "e4m3": ord("E")}
 _EPI = {"none": ord("n"), "relu": ord("r"), "bias_relu": ord("b")}
-_NP_BITS = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16}
+_NP_BITS = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8}
 
 _lock = threading.Lock()
 _lib = None
@@ -110,19 +110,20 @@ def encode(x: np.ndarray, dtype: str) -> np.ndarray:
     return out
 
 
-def _check_operands(A_bits, B_bits, K):
+def _check_operands(A_bits, B_bits, in_dtype):
     if A_bits.ndim != 2 or B_bits.ndim != 2:
         raise ValueError("A and B must be 2-D bit arrays")
-    if A_bits.dtype != np.uint16 or B_bits.dtype != np.uint16:
-        raise ValueError("A and B hold 16-bit patterns (uint16)")
+    want = _NP_BITS[in_dtype]
+    if A_bits.dtype != want or B_bits.dtype != want:
+        raise ValueError(f"A and B hold {in_dtype} patterns ({np.dtype(want).name})")
     for X in (A_bits, B_bits):
-        if X.size > 0 and X.shape[1] > 1 and X.strides[1] != 2:
+        if X.size > 0 and X.shape[1] > 1 and X.strides[1] != X.itemsize:
             raise ValueError("rows of A and B must be contiguous")
 
 
 def _ld(X) -> int:
     """Row pitch in elements (a degenerate array gets its width)."""
-    return max(X.strides[0] // 2, X.shape[1]) if X.size > 0 and X.shape[0] > 1 else X.shape[1]
+    return max(X.strides[0] // X.itemsize, X.shape[1]) if X.size > 0 and X.shape[0] > 1 else X.shape[1]
 
 
 def _residual(R_bits, r_dtype, N):
@@ -148,7 +149,7 @@ def gemm(A_bits: np.ndarray, B_bits: np.ndarray, in_dtype: str, out_dtype: str, 
     C_init's width, whose padding is kept untouched; else N), C_exact the
     fp64 value before the final rounding and S the sum of |a_ik b_kj|, both
     M x N."""
-    _check_operands(A_bits, B_bits, K)
+    _check_operands(A_bits, B_bits, in_dtype)
     M = A_bits.shape[0]
     K = A_bits.shape[1] if K is None else int(K)
     N = B_bits.shape[1] if N is None else int(N)
@@ -178,7 +179,7 @@ def gemm_at(A_bits: np.ndarray, B_bits: np.ndarray, rows, cols, in_dtype: str, o
             threads: int | None = None, R_bits: np.ndarray | None = None, r_dtype: str | None = None):
     """The same definition at the positions (rows[t], cols[t]) only.
     Returns (C_bits, C_exact, S) as 1-D arrays over t."""
-    _check_operands(A_bits, B_bits, K)
+    _check_operands(A_bits, B_bits, in_dtype)
     M = A_bits.shape[0]
     K = A_bits.shape[1] if K is None else int(K)
     N = B_bits.shape[1] if N is None else int(N)

@@ -13,6 +13,8 @@
  * binary16/binary32 and bfloat16 bit layouts, and its own type codes.
  *
  * What each piece follows:
+ *   - Operand types: gizml:tile, "F16", "BF16" and "FP8" ("FP8 E4M3
+ *     floats") are the storage types of the matrix-core operands.
  *   - The product itself: gizml:tile, "Tile.dot" -- the matrix product
  *     [M,K][K,N] -> [M,N] kept in F32; here it is kept in fp64 so that the
  *     GPU's F32 accumulation is graded against the (almost) exact sum.
@@ -59,6 +61,8 @@
 #define ORC_FP32 'S' /* IEEE 754 binary32 */
 #define ORC_FP16 'H' /* IEEE 754 binary16 */
 #define ORC_BF16 'B' /* bfloat16: binary32's sign and exponent, 7 fraction bits */
+#define ORC_E4M3 'E' /* OCP FP8 E4M3: 4 exponent bits (bias 7), 3 fraction bits, no
+                        infinities, NaN only at S.1111.111, largest finite 448 */
 
 #define ORC_EPI_NONE 'n'
 #define ORC_EPI_RELU 'r'
@@ -72,6 +76,7 @@ static int fmt_fields(int dtype, int *ebits, int *fbits) {
     case ORC_FP32: *ebits = 8; *fbits = 23; return 0;
     case ORC_FP16: *ebits = 5; *fbits = 10; return 0;
     case ORC_BF16: *ebits = 8; *fbits = 7; return 0;
+    case ORC_E4M3: *ebits = 4; *fbits = 3; return 0;
     default: return -1;
     }
 }
@@ -90,7 +95,10 @@ double orc_decode(int dtype, uint32_t bits) {
     const uint32_t e = (bits >> fbits) & emask;
     const uint32_t f = bits & fmask;
     double mag;
-    if (e == emask) {
+    if (dtype == ORC_E4M3 && e == emask) {
+        /* E4M3 keeps the all-ones exponent for finite values; only f = 7 is NaN */
+        mag = (f == fmask) ? NAN : ldexp((double)((1u << fbits) | f), (int)e - bias - fbits);
+    } else if (e == emask) {
         mag = (f == 0) ? INFINITY : NAN;
     } else if (e == 0) {
         mag = ldexp((double)f, 1 - bias - fbits);
@@ -105,6 +113,7 @@ double orc_decode(int dtype, uint32_t bits) {
  * infinity; NaN becomes the quiet NaN with x's sign. */
 uint32_t orc_encode(int dtype, double x) {
     int ebits, fbits;
+    if (dtype == ORC_E4M3) return 0; /* E4M3 is an operand type only: never encoded */
     if (fmt_fields(dtype, &ebits, &fbits) != 0) return 0;
     const uint32_t emask = (1u << ebits) - 1u;
     const int bias = (int)(emask >> 1);
@@ -139,6 +148,7 @@ uint32_t orc_encode(int dtype, double x) {
 }
 
 static uint32_t load_bits(int dtype, const void *p, int64_t idx) {
+    if (dtype == ORC_E4M3) return ((const unsigned char *)p)[idx];
     if (dtype == ORC_FP32) {
         uint32_t v;
         memcpy(&v, (const unsigned char *)p + 4 * idx, 4);
@@ -223,7 +233,7 @@ static void *gemm_rows(void *arg) {
     return NULL;
 }
 
-static int valid_in(int d) { return d == ORC_FP16 || d == ORC_BF16; }
+static int valid_in(int d) { return d == ORC_FP16 || d == ORC_BF16 || d == ORC_E4M3; }
 static int valid_out(int d) { return d == ORC_FP32 || d == ORC_FP16 || d == ORC_BF16; }
 static int valid_epi(int e) { return e == ORC_EPI_NONE || e == ORC_EPI_RELU || e == ORC_EPI_BIAS_RELU; }
 

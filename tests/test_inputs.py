@@ -60,3 +60,20 @@ def test_workload_table():
     a = gi.WORKLOADS["ragged1000_f16"].a_bits(ld=1008)
     assert a.shape == (1000, 1008) and np.all(a[:, 1000:] == 0)
     assert np.array_equal(a[:, :1000], gi.WORKLOADS["ragged1000_f16"].a_bits())
+
+
+def test_e4m3_storage_rounding():
+    torch = __import__("pytest").importorskip("torch")
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.normal(0, 50, 20000), rng.normal(0, 0.01, 20000), [0.0, -0.0, 448.0, -448.0,
+                        2.0 ** -10, 3 * 2.0 ** -10, 1.0625, 1.1875, 2.0 ** -6]])
+    ours = gi.to_storage_bits(x, "e4m3")
+    within = np.abs(x) <= 448.0
+    # inside the finite range torch's float32 -> e4m3fn cast rounds to nearest even
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours[within], ref[within])
+    # beyond it the generator saturates (torch would give NaN)
+    big = gi.to_storage_bits(np.array([449.0, 1e6, -1e6, 500.0]), "e4m3")
+    assert list(big) == [0x7E, 0x7E, 0xFE, 0x7E]
+    # ties to even: 1.0625 is halfway between 1 (even) and 1.125; 1.1875 between 1.125 and 1.25 (even)
+    assert list(gi.to_storage_bits(np.array([1.0625, 1.1875]), "e4m3")) == [0x38, 0x3A]

@@ -33,7 +33,7 @@ def test_decode_golden(oracle_mod):
     rows = _read_formats()
     assert len(rows) >= 20
     for dt, bits, mant, e in rows:
-        arr = np.array([bits], dtype=np.uint32 if dt == "f32" else np.uint16)
+        arr = np.array([bits], dtype={"f32": np.uint32, "e4m3": np.uint8}.get(dt, np.uint16))
         got = oracle_mod.decode(arr, dt)[0]
         want = float(np.ldexp(float(mant), e))
         assert got == want, (dt, hex(bits), got, want)
@@ -43,6 +43,8 @@ def test_decode_golden(oracle_mod):
 
 def test_encode_golden_roundtrip(oracle_mod):
     for dt, bits, mant, e in _read_formats():
+        if dt == "e4m3":
+            continue  # an operand type only: the oracle never encodes it
         got = oracle_mod.encode(np.array([np.ldexp(float(mant), e)]), dt)[0]
         assert int(got) == bits, (dt, hex(bits), hex(int(got)))
 
@@ -491,3 +493,46 @@ def test_tolerance_added_term(oracle_mod):
     t0 = oracle_mod.tolerance(np.array([0.0]), np.array([1.0]), "f32")
     t1 = oracle_mod.tolerance(np.array([0.0]), np.array([1.0]), "f32", added=np.array([2.0 ** 20]))
     assert t1[0] - t0[0] == pytest.approx(2.0 ** -3)
+
+
+# ------------------------------------------------------------ FP8 E4M3
+
+def test_decode_all_e4m3_vs_torch(oracle_mod):
+    torch = pytest.importorskip("torch")
+    bits = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    ours = oracle_mod.decode(bits, "e4m3")
+    ref = torch.from_numpy(bits.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def _e4m3(x):
+    return gemm_inputs.to_storage_bits(np.asarray(x, dtype=np.float64), "e4m3")
+
+
+def test_e4m3_integer_inputs_exact(oracle_mod):
+    rng = np.random.default_rng(90)
+    M, N, K = 23, 31, 512
+    Ai = rng.integers(-8, 9, (M, K))        # every integer in [-16, 16] is exact in E4M3
+    Bi = rng.integers(-8, 9, (K, N))
+    C, exact, S = oracle_mod.gemm(_e4m3(Ai), _e4m3(Bi), "e4m3", "f32")
+    assert np.array_equal(exact, (Ai @ Bi).astype(np.float64))
+    assert np.array_equal(S, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (5, 7, 33), (17, 16, 64), (9, 40, 130)])
+def test_e4m3_brute_force_vs_float64_matmul(oracle_mod, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    A = _e4m3(rng.normal(0, 2, (M, K)))
+    B = _e4m3(rng.normal(0, 2, (K, N)))
+    Ad, Bd = oracle_mod.decode(A, "e4m3"), oracle_mod.decode(B, "e4m3")
+    _, exact, _ = oracle_mod.gemm(A, B, "e4m3", "f32")
+    np.testing.assert_allclose(exact, Ad @ Bd, rtol=1e-13, atol=1e-13)
+
+
+def test_e4m3_identity_exact(oracle_mod):
+    rng = np.random.default_rng(91)
+    A = _e4m3(rng.normal(0, 10, (20, 48)))
+    C, exact, _ = oracle_mod.gemm(A, _e4m3(np.eye(48)), "e4m3", "f32")
+    assert np.array_equal(exact, oracle_mod.decode(A, "e4m3"))
