@@ -17,7 +17,7 @@ Generator (counter-based, so any element can be drawn independently):
     storage type: fp16 directly; bf16 through binary32 (float64 -> float32
     RNE, then float32 -> bf16 RNE on the bit pattern); fp32 bias directly.
 
-Streams: A = 0, B = 1, bias = 2, residual = 3.  Workload w (1..6) uses seed
+Streams: A = 0, B = 1, bias = 2, residual = 3.  Workload w (1..7) uses seed
 1000 + w.
 """
 from __future__ import annotations
@@ -159,7 +159,8 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Each operand read once and C written once (bias included)."""
         out_size = {"f32": 4, "f16": 2, "bf16": 2}[self.out_dtype]
-        b = 2 * self.M * self.K + 2 * self.K * self.N + out_size * self.M * self.N
+        in_size = 1 if self.in_dtype == "e4m3" else 2
+        b = in_size * (self.M * self.K + self.K * self.N) + out_size * self.M * self.N
         if self.epilogue == "bias_relu":
             b += 4 * self.N
         if self.dist_r is not None:
@@ -198,6 +199,10 @@ WORKLOADS = {
         "square8192_bf16", 8192, 8192, 8192, "bf16", "bf16", "none",
         ("uniform", -1.0, 1.0), ("uniform", -1.0, 1.0), None, 1003,
         "bf16 M=N=K=8192, uniform[-1,1), fp32 accumulate, bf16 output, no epilogue"),
+    "square8192_e4m3": Workload(
+        "square8192_e4m3", 8192, 8192, 8192, "e4m3", "bf16", "none",
+        ("uniform", -1.0, 1.0), ("uniform", -1.0, 1.0), None, 1007,
+        "FP8 E4M3 M=N=K=8192, uniform[-1,1) rounded to E4M3, fp32 accumulate, bf16 output, no epilogue"),
     "relu4096_f16": Workload(
         "relu4096_f16", 4096, 4096, 4096, "f16", "f16", "relu",
         ("normal", 0.0, 1.0 / 64.0), ("normal", 0.0, 1.0 / 64.0), None, 1004,

@@ -5,11 +5,13 @@
  *
  * A is M x K, B is K x N, C is M x N, all row-major with leading dimensions
  * (row pitches, in elements) lda >= K, ldb >= N, ldc >= N.  A and B are both
- * fp16 or both bf16; the product is accumulated in fp32; C is fp32, fp16 or
- * bf16.  The operation and its rules come from these pages:
+ * fp16, both bf16 or both FP8 E4M3; the product is accumulated in fp32; C is
+ * fp32, fp16 or bf16.  The operation and its rules come from these pages:
  *
  *   - gizml:tile, "Tile.dot": the matrix product [M,K][K,N] -> [M,N] in F32,
- *     on matrix cores when both operands are F16 or both are BF16.
+ *     on matrix cores when both operands are F16 or both are BF16; "FP8" is
+ *     the page's fourth storage type (E4M3), taken here as a third operand
+ *     type of one kind for both operands (tcgen05 kind::f8f6f4).
  *   - gizml:tile, "Tile.run" (the fused example over 128 x 128 output tiles,
  *     storing acc.relu()), "Tile.relu" and "Tile.add": the epilogues.  The
  *     bias of SG_EPI_BIAS_RELU is one fp32 value per column, added to the
@@ -59,7 +61,8 @@ extern "C" {
 enum {
     SG_F32 = 0,  /* IEEE binary32 (output only) */
     SG_F16 = 1,  /* IEEE binary16 */
-    SG_BF16 = 2  /* bfloat16 */
+    SG_BF16 = 2, /* bfloat16 */
+    SG_E4M3 = 3  /* OCP FP8 E4M3 (operands only; gizml:tile, "FP8") */
 };
 
 /* Epilogues applied to the fp32 accumulator before the output rounding. */
@@ -75,7 +78,7 @@ enum {
     SG_ERR_ARG = -1,     /* M, N or K < 0; ld < row length; null pointer; bias
                             missing for SG_EPI_BIAS_RELU or given otherwise;
                             a dimension or pitch beyond 2^31 - 1 */
-    SG_ERR_DTYPE = -2,   /* in_dtype not fp16/bf16, out_dtype not fp32/fp16/bf16,
+    SG_ERR_DTYPE = -2,   /* in_dtype not fp16/bf16/e4m3, out_dtype not fp32/fp16/bf16,
                             or an unknown epilogue */
     SG_ERR_STAGES = -3,  /* stages < 0, > SG_MAX_STAGES, or does not fit in
                             shared memory for the chosen tile */
@@ -98,7 +101,7 @@ enum {
  *   A, lda      device pointer to M x K row-major in_dtype elements; lda >= K.
  *   B, ldb      device pointer to K x N row-major in_dtype elements; ldb >= N.
  *   C, ldc      device pointer to M x N row-major out_dtype elements; ldc >= N.
- *   in_dtype    SG_F16 or SG_BF16 (both operands).
+ *   in_dtype    SG_F16, SG_BF16 or SG_E4M3 (both operands).
  *   out_dtype   SG_F32, SG_F16 or SG_BF16.
  *   epilogue    SG_EPI_NONE, SG_EPI_RELU or SG_EPI_BIAS_RELU.
  *   bias        device pointer to N fp32 values, required iff BIAS_RELU.
@@ -107,11 +110,12 @@ enum {
  *   stream      cudaStream_t (as void*) the work is queued on.
  *
  * Layouts: an operand whose base is 16-byte aligned and whose row pitch is
- * a multiple of 16 bytes (lda, ldb multiples of 8 elements; any pitch for a
- * single row) is staged by TMA.  Any other operand is staged by element
+ * a multiple of 16 bytes (lda, ldb multiples of 8 elements, of 16 for FP8;
+ * any pitch for a single row) is staged by TMA.  Any other operand is staged by element
  * loads of the producer warp into the same shared-memory layout (slower; the
  * kernel then runs one CTA per tile); the results are bit-identical.  Only
- * element alignment (2 bytes) is required, else SG_ERR_ALIGN.  C has no
+ * element alignment (2 bytes for 16-bit operands) is required, else
+ * SG_ERR_ALIGN.  C has no
  * alignment rule: a C that is not 16-byte aligned or whose pitch is not a
  * multiple of 16 bytes gets masked element stores instead of TMA stores.
  */
@@ -151,7 +155,7 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K,
 typedef struct {
     int32_t block_m;       /* output tile rows (128) */
     int32_t block_n;       /* output tile columns */
-    int32_t block_k;       /* K elements per stage (64) */
+    int32_t block_k;       /* K elements per stage (64, or 128 for FP8) */
     int32_t stages;        /* operand slots in the shared-memory ring */
     int32_t max_stages;    /* the largest count that fits for this tile */
     int32_t tiles;         /* output tiles */

@@ -23,7 +23,7 @@ from . import _build
 LIB_PATH = _build.LIB
 
 # Storage-type and epilogue codes of the C ABI.
-SG_F32, SG_F16, SG_BF16 = 0, 1, 2
+SG_F32, SG_F16, SG_BF16, SG_E4M3 = 0, 1, 2, 3
 EPILOGUES = {"none": 0, "relu": 1, "bias_relu": 2}
 SG_MAX_STAGES = 8
 
@@ -117,6 +117,8 @@ def _torch():
 def dtype_code(dt) -> int:
     torch = _torch()
     codes = {torch.float32: SG_F32, torch.float16: SG_F16, torch.bfloat16: SG_BF16}
+    if hasattr(torch, "float8_e4m3fn"):
+        codes[torch.float8_e4m3fn] = SG_E4M3
     if dt not in codes:
         raise ValueError(f"unsupported dtype {dt}")
     return codes[dt]

@@ -41,8 +41,8 @@ struct DevState {
     int major = 0, minor = 0;
     int* status = nullptr;  // device status word (4 bytes, library-owned)
     // per kernel instantiation [tile width][output type][mode - 1][residual]:
-    bool attr_done[3][3][3][2] = {};    // dynamic shared-memory attribute set
-    int max_clusters[3][3][3][2] = {};  // co-resident clusters (0: not queried)
+    bool attr_done[2][3][3][3][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
+    int max_clusters[2][3][3][3][2] = {};  // the same index: co-resident clusters (0: not queried)
 };
 
 std::mutex g_mu;
@@ -65,8 +65,8 @@ std::atomic<uint64_t> g_wait_limit_ns{initial_wait_limit()};
 std::atomic<int64_t> g_skip_load{-1};
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-int elem_bytes(int dt) { return dt == SG_F32 ? 4 : 2; }
-bool valid_in(int dt) { return dt == SG_F16 || dt == SG_BF16; }
+int elem_bytes(int dt) { return dt == SG_F32 ? 4 : dt == SG_E4M3 ? 1 : 2; }
+bool valid_in(int dt) { return dt == SG_F16 || dt == SG_BF16 || dt == SG_E4M3; }
 bool valid_out(int dt) { return dt == SG_F32 || dt == SG_F16 || dt == SG_BF16; }
 bool valid_epi(int e) { return e == SG_EPI_NONE || e == SG_EPI_RELU || e == SG_EPI_BIAS_RELU; }
 
@@ -97,20 +97,23 @@ int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
     if (cdiv(M, sg::BM) * cdiv(N, 64) > lim) return SG_ERR_ARG;
     const uint64_t c_span = span_bytes(M, N, ldc, elem_bytes(out_dtype));
     if (K > 0) {
-        if (overlap(C, c_span, A, span_bytes(M, K, lda, 2)) || overlap(C, c_span, B, span_bytes(K, N, ldb, 2)))
+        const int ies = elem_bytes(in_dtype);
+        if (overlap(C, c_span, A, span_bytes(M, K, lda, ies)) || overlap(C, c_span, B, span_bytes(K, N, ldb, ies)))
             return SG_ERR_ALIAS;
     }
     if (bias && overlap(C, c_span, bias, static_cast<uint64_t>(N) * 4)) return SG_ERR_ALIAS;
     // 16-bit elements must sit on 2-byte boundaries; anything coarser is
     // handled (TMA when legal, element loads otherwise)
-    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 1) || (reinterpret_cast<uintptr_t>(B) & 1))) return SG_ERR_ALIGN;
+    const uintptr_t emask = static_cast<uintptr_t>(elem_bytes(in_dtype) - 1);
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & emask) || (reinterpret_cast<uintptr_t>(B) & emask)))
+        return SG_ERR_ALIGN;
     return SG_OK;
 }
 
 // An operand can be copied by TMA when its base is 16-byte aligned and its
 // row pitch is a multiple of 16 bytes (a single row has no pitch).
-bool tma_legal(const void* X, int64_t rows, int64_t ld) {
-    return (reinterpret_cast<uintptr_t>(X) & 15) == 0 && (rows <= 1 || (ld * 2) % 16 == 0);
+bool tma_legal(const void* X, int64_t rows, int64_t ld, int esz) {
+    return (reinterpret_cast<uintptr_t>(X) & 15) == 0 && (rows <= 1 || (ld * esz) % 16 == 0);
 }
 
 int ensure_encode_fn() {
@@ -167,6 +170,7 @@ TuneKey tune_key(int dev, int64_t M, int64_t N, int64_t K, int in_dtype, int out
 
 struct Plan {
     int bn = 128;
+    int block_k = 64;  // K elements per stage (128 bytes of K)
     int group_m = 8;
     int mode = 1;  // 1: single CTA, 2: CTA pairs sharing B by multicast, 3: paired MMA
     int cm = 1;    // CTAs per cluster along M
@@ -215,12 +219,15 @@ std::atomic<int> g_force_mode{[] {
     return (x >= 1 && x <= 3) ? x : 0;
 }()};
 
-int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype, const void* C, int64_t ldc,
-              int stages, bool a_tma, bool b_tma, Plan* pl, const Choice* choice = nullptr) {
+int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, const void* C,
+              int64_t ldc, int stages, bool a_tma, bool b_tma, Plan* pl, const Choice* choice = nullptr) {
+    const int esz = elem_bytes(in_dtype);
+    const int boxc = 128 / esz;  // B columns per 128-byte box: tile widths and CTA shares are multiples
     pl->a_tma = a_tma ? 1 : 0;
     pl->b_tma = b_tma ? 1 : 0;
     pl->m_blocks = cdiv(M, sg::BM);
-    pl->k_chunks = cdiv(K, sg::BK);
+    pl->block_k = sg::BK_BYTES / esz;
+    pl->k_chunks = cdiv(K, pl->block_k);
     // Tile width: the widest of 256 / 192 / 128 that covers N as tightly as
     // 128 does (no more padded columns) and still gives every SM a tile.  A
     // short K loop (<= 4 chunks) makes the epilogue the bottleneck: keep 128,
@@ -228,6 +235,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
     int bn = 128;
     const double eff128 = static_cast<double>(N) / (cdiv(N, 128) * 128.0);
     for (int cand : {256, 192}) {
+        if (cand % boxc) continue;
         if (pl->k_chunks <= 4) break;
         if (N < cand) continue;
         const double eff = static_cast<double>(N) / (cdiv(N, cand) * static_cast<double>(cand));
@@ -244,7 +252,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
     // Pairs of CTAs compute 256-row tiles with the paired MMA when the
     // problem is large and the K loop long enough for operand traffic to
     // matter: each SM then stages only its half of B.
-    const bool pairable = (bn / 64) % 2 == 0;
+    const bool pairable = (bn / boxc) % 2 == 0;  // each CTA of a pair owns whole boxes of B
     int mode = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pl->m_blocks * pl->n_blocks >= st.sm_count && pairable)
                    ? 3
                    : 1;
@@ -279,6 +287,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int out_dtype
 
 CUtensorMapDataType tmap_dtype(int dt) {
     switch (dt) {
+        case SG_E4M3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;  // bytes are moved, never interpreted
         case SG_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         case SG_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -306,7 +315,9 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
                 const CUtensorMap& tc, const CUtensorMap& tr, const sg::Params& prm, bool residual,
                 cudaStream_t stream) {
     sg::LaunchFn fn = nullptr;
-    if (pl.mode == 1)
+    if (pl.block_k == sg::BK_BYTES)  // 8-bit operands
+        fn = residual ? sg::launcher_fp8_res(pl.bn, out_dtype, pl.mode) : sg::launcher_fp8_plain(pl.bn, out_dtype, pl.mode);
+    else if (pl.mode == 1)
         fn = residual ? sg::launcher_res_single(pl.bn, out_dtype) : sg::launcher_plain_single(pl.bn, out_dtype);
     else
         fn = residual ? sg::launcher_res_pair(pl.bn, out_dtype, pl.mode)
@@ -324,8 +335,9 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
     a.smem_optin = st.smem_optin;
     a.stream = stream;
     a.mu = &g_mu;
-    a.attr_done = &st.attr_done[bi][out_dtype][pl.mode - 1][residual ? 1 : 0];
-    a.max_clusters = &st.max_clusters[bi][out_dtype][pl.mode - 1][residual ? 1 : 0];
+    const int e8 = pl.block_k == sg::BK_BYTES ? 1 : 0;
+    a.attr_done = &st.attr_done[e8][bi][out_dtype][pl.mode - 1][residual ? 1 : 0];
+    a.max_clusters = &st.max_clusters[e8][bi][out_dtype][pl.mode - 1][residual ? 1 : 0];
     return fn(a) == 0 ? SG_OK : SG_ERR_CUDA;
 }
 
@@ -335,7 +347,7 @@ void fill_info(const Plan& pl, sg_plan_info* info) {
     std::memset(info, 0, sizeof(*info));
     info->block_m = sg::BM;
     info->block_n = pl.bn;
-    info->block_k = sg::BK;
+    info->block_k = static_cast<int32_t>(pl.block_k);
     info->stages = pl.stages;
     info->max_stages = pl.max_stages;
     info->tiles = static_cast<int32_t>(pl.tiles);
@@ -373,15 +385,16 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
                     int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
                     int stages, int64_t skip_load, cudaStream_t stream, const Choice* forced = nullptr,
                     Plan* used = nullptr, const void* R = nullptr, int64_t ldr = 0) {
-    const bool a_tma = tma_legal(A, M, lda);
-    const bool b_tma = tma_legal(B, K, ldb);
+    const int esz = elem_bytes(in_dtype);
+    const bool a_tma = tma_legal(A, M, lda, esz);
+    const bool b_tma = tma_legal(B, K, ldb, esz);
     Choice tuned;
     const Choice* choice = forced;
     if (!choice && lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, a_tma, b_tma,
                                 c_tma_legal(C, M, ldc, out_dtype), &tuned))
         choice = &tuned;
     Plan pl;
-    int rc = make_plan(st, M, N, K, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice);
+    int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice);
     if (rc != SG_OK) return rc;
     if (used) *used = pl;
 
@@ -391,8 +404,9 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     std::memset(&tc, 0, sizeof(tc));
     std::memset(&tr, 0, sizeof(tr));
     if (K > 0) {
-        if (a_tma && (rc = encode_2d(&ta, in_dtype, A, K, M, lda * 2, sg::BK, sg::BM)) != SG_OK) return rc;
-        if (b_tma && (rc = encode_2d(&tb, in_dtype, B, N, K, ldb * 2, 64, sg::BK)) != SG_OK) return rc;
+        const uint32_t kb = sg::BK_BYTES / esz, boxc = 128 / esz;
+        if (a_tma && (rc = encode_2d(&ta, in_dtype, A, K, M, lda * esz, kb, sg::BM)) != SG_OK) return rc;
+        if (b_tma && (rc = encode_2d(&tb, in_dtype, B, N, K, ldb * esz, boxc, kb)) != SG_OK) return rc;
     }
     const int oes = elem_bytes(out_dtype);
     if (pl.tma_store) {
@@ -413,7 +427,9 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
     prm.group_m = pl.group_m;
-    prm.idesc = sg::idesc_f16(in_dtype == SG_BF16, pl.mode == 3 ? 2 * sg::BM : sg::BM, pl.bn, true);
+    const int mma_m = pl.mode == 3 ? 2 * sg::BM : sg::BM;
+    prm.idesc = esz == 1 ? sg::idesc_e4m3(mma_m, pl.bn, true)
+                         : sg::idesc_f16(in_dtype == SG_BF16, mma_m, pl.bn, true);
     prm.epi = epilogue;
     prm.tma_store = pl.tma_store;
     prm.bias = bias;
@@ -482,7 +498,8 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
     Choice tuned;
     const bool have = lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, true, true,
                                    c_tma_legal(C, M, ldc, out_dtype), &tuned);
-    if ((rc = make_plan(*st, M, N, K, out_dtype, C, ldc, stages, true, true, &pl, have ? &tuned : nullptr)) != SG_OK)
+    if ((rc = make_plan(*st, M, N, K, in_dtype, out_dtype, C, ldc, stages, true, true, &pl, have ? &tuned : nullptr)) !=
+        SG_OK)
         return rc;
     fill_info(pl, info);
     return SG_OK;
@@ -497,16 +514,18 @@ int sg_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
     DevState* st = nullptr;
     if ((rc = device_state(&st)) != SG_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool a_tma = tma_legal(A, M, lda), b_tma = tma_legal(B, K, ldb);
+    const int esz = elem_bytes(in_dtype);
+    const bool a_tma = tma_legal(A, M, lda, esz), b_tma = tma_legal(B, K, ldb, esz);
     const bool c_tma = c_tma_legal(C, M, ldc, out_dtype);
     const int64_t m_blocks = cdiv(M, sg::BM);
 
     // the configurations that fit this problem
     std::vector<Choice> cands;
     for (int bn : {128, 192, 256}) {
+        if (bn % (128 / esz)) continue;  // whole 128-byte B boxes
         if (bn > 128 && N <= bn - 64) continue;  // a tile mostly past N
         for (int mode : {1, 2, 3}) {
-            if (mode > 1 && ((bn / 64) % 2 != 0 || m_blocks < 2 || !a_tma || !b_tma)) continue;
+            if (mode > 1 && ((bn / (128 / esz)) % 2 != 0 || m_blocks < 2 || !a_tma || !b_tma)) continue;
             for (int g : {4, 8, 16}) {
                 Choice c;
                 c.bn = bn;

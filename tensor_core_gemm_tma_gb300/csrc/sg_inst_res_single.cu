@@ -5,15 +5,15 @@ namespace sg {
 
 LaunchFn launcher_res_single(int bn, int out) {
     switch (bn * 4 + out) {
-        case 128 * 4 + SG_F32: return &launch_kernel<128, SG_F32, 1, true>;
-        case 128 * 4 + SG_F16: return &launch_kernel<128, SG_F16, 1, true>;
-        case 128 * 4 + SG_BF16: return &launch_kernel<128, SG_BF16, 1, true>;
-        case 192 * 4 + SG_F32: return &launch_kernel<192, SG_F32, 1, true>;
-        case 192 * 4 + SG_F16: return &launch_kernel<192, SG_F16, 1, true>;
-        case 192 * 4 + SG_BF16: return &launch_kernel<192, SG_BF16, 1, true>;
-        case 256 * 4 + SG_F32: return &launch_kernel<256, SG_F32, 1, true>;
-        case 256 * 4 + SG_F16: return &launch_kernel<256, SG_F16, 1, true>;
-        case 256 * 4 + SG_BF16: return &launch_kernel<256, SG_BF16, 1, true>;
+        case 128 * 4 + SG_F32: return &launch_kernel<128, SG_F32, 1, true, 2>;
+        case 128 * 4 + SG_F16: return &launch_kernel<128, SG_F16, 1, true, 2>;
+        case 128 * 4 + SG_BF16: return &launch_kernel<128, SG_BF16, 1, true, 2>;
+        case 192 * 4 + SG_F32: return &launch_kernel<192, SG_F32, 1, true, 2>;
+        case 192 * 4 + SG_F16: return &launch_kernel<192, SG_F16, 1, true, 2>;
+        case 192 * 4 + SG_BF16: return &launch_kernel<192, SG_BF16, 1, true, 2>;
+        case 256 * 4 + SG_F32: return &launch_kernel<256, SG_F32, 1, true, 2>;
+        case 256 * 4 + SG_F16: return &launch_kernel<256, SG_F16, 1, true, 2>;
+        case 256 * 4 + SG_BF16: return &launch_kernel<256, SG_BF16, 1, true, 2>;
         default: return nullptr;
     }
 }

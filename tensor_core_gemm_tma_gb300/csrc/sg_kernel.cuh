@@ -69,10 +69,22 @@
 namespace sg {
 
 constexpr int BM = 128;                 // tile rows = MMA M = tensor-memory lanes
-constexpr int BK = 64;                  // K elements per stage: one 128-byte swizzle row of 16-bit values
-constexpr int UMMA_K = 16;              // K per tcgen05.mma.kind::f16
-constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int B_CHUNK_BYTES = BK * 64 * 2;  // one TMA box of B: 64 K-rows x 64 N-columns
+// Operand geometry in bytes is the same for 16-bit (ESZ = 2) and 8-bit
+// (ESZ = 1) elements: a stage holds one 128-byte swizzle row of K per A row
+// (64 or 128 elements), an MMA consumes 32 bytes of K (16 or 32 elements),
+// a B box is 128 bytes of N (64 or 128 columns) by the stage's K rows.
+constexpr int BK_BYTES = 128;
+constexpr int A_STAGE_BYTES = BM * BK_BYTES;
+template <int ESZ>
+struct Geom {
+    static_assert(ESZ == 1 || ESZ == 2, "8- or 16-bit operands");
+    static constexpr int KB = BK_BYTES / ESZ;        // K elements per stage
+    static constexpr int UK = 32 / ESZ;              // K elements per MMA
+    static constexpr int BOXC = 128 / ESZ;           // B columns per TMA box
+    static constexpr int B_BOX_BYTES = KB * 128;     // one B box: KB rows x 128 bytes
+    static constexpr int B_KSTEP_BYTES = UK * 128;   // B descriptor advance per MMA (UK rows)
+};
+constexpr int BK = Geom<2>::KB;  // K elements per stage for 16-bit operands
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int EPI_BUF_BYTES = 32 * 128;     // one warp's staging buffer: 32 rows x 128 bytes
@@ -92,7 +104,8 @@ template <int BN, int BL = BN>
 struct Layout {
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
     static_assert(BL % 64 == 0 && BL <= BN, "B is staged in whole 64-column boxes");
-    static constexpr int B_STAGE_BYTES = BK * BL * 2;
+    // B per stage: BL columns x KB rows of ESZ bytes = BL x 128 bytes for either element size
+    static constexpr int B_STAGE_BYTES = BK_BYTES * BL;
     static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
     static constexpr int ACC = (TMEM_COLS / BN) < MAX_ACC ? (TMEM_COLS / BN) : MAX_ACC;
     static __host__ __device__ constexpr int epi_offset(int stages) { return stages * STAGE_BYTES; }
@@ -121,8 +134,8 @@ struct Params {
     // pitch that is not a multiple of 16 bytes) are copied by the producer
     // warp with element loads instead (single-CTA mode only).
     int32_t a_tma, b_tma;  // 1: copied by TMA, 0: by element loads
-    const uint16_t* A;     // 16-bit elements; used when a_tma == 0
-    const uint16_t* B;     // used when b_tma == 0
+    const void* A;         // used when a_tma == 0
+    const void* B;         // used when b_tma == 0
     int64_t lda, ldb;
     // Residual R (M x N, the output's type), added to the accumulator before
     // the bias and the ReLU; may be C itself (same address and pitch).
@@ -131,11 +144,24 @@ struct Params {
     int32_t r_tma;         // 1: R tiles are loaded by TMA, 0: by element loads
 };
 
-// Element-load staging of one A chunk (rows m0.., k0..k0+63) into the same
-// 128-byte-swizzled K-major layout the TMA box produces: row r at r * 128,
-// 16-byte chunk c of it at c ^ (r mod 8).  Out-of-range elements are
-// written as 0 (Tolk.Stage: a gate whose index fails copies 0).  Whole warp.
+template <int ESZ>
+__device__ __forceinline__ uint32_t load_elem(const void* X, int64_t idx) {
+    if constexpr (ESZ == 2) {
+        return __ldg(static_cast<const uint16_t*>(X) + idx);
+    } else {
+        return __ldg(static_cast<const uint8_t*>(X) + idx);
+    }
+}
+
+// Element-load staging of one A chunk (rows m0.., one stage of K from k0)
+// into the same 128-byte-swizzled K-major layout the TMA box produces: row r
+// at r * 128, 16-byte chunk c of it at c ^ (r mod 8).  Out-of-range elements
+// are written as 0 (Tolk.Stage: a gate whose index fails copies 0).  Whole
+// warp.
+template <int ESZ>
 __device__ __forceinline__ void copy_a_elements(uint32_t dst, const Params& p, int m0, int k0, int lane) {
+    constexpr int EPW = 4 / ESZ;   // elements per 32-bit word
+    constexpr int EPC = 16 / ESZ;  // elements per 16-byte chunk
 #pragma unroll 1
     for (int c = lane; c < BM * 8; c += 32) {
         const int r = c >> 3, ch = c & 7;
@@ -143,11 +169,14 @@ __device__ __forceinline__ void copy_a_elements(uint32_t dst, const Params& p, i
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int k = k0 + ch * 8 + 2 * e;
-            const uint16_t* src = p.A + static_cast<int64_t>(row) * p.lda + k;
-            const uint32_t lo = (row < p.M && k < p.K) ? __ldg(src) : 0u;
-            const uint32_t hi = (row < p.M && k + 1 < p.K) ? __ldg(src + 1) : 0u;
-            w[e] = lo | (hi << 16);
+            uint32_t word = 0;
+#pragma unroll
+            for (int t = 0; t < EPW; ++t) {
+                const int k = k0 + ch * EPC + e * EPW + t;
+                if (row < p.M && k < p.K)
+                    word |= load_elem<ESZ>(p.A, static_cast<int64_t>(row) * p.lda + k) << (8 * ESZ * t);
+            }
+            w[e] = word;
         }
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + r * 128 + ((ch ^ (r & 7)) << 4)),
                      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
@@ -155,26 +184,33 @@ __device__ __forceinline__ void copy_a_elements(uint32_t dst, const Params& p, i
     }
 }
 
-// The same for one B chunk (K rows k0..k0+63, columns n0..n0+ncols-1) into
-// the MN-major layout of the TMA boxes: 64-column box j at j * 8 KiB, K row
-// kr at kr * 128, 16-byte chunk c of it at c ^ (kr mod 8).
+// The same for one B chunk (one stage of K rows from k0, columns n0..n0+ncols-1)
+// into the MN-major layout of the TMA boxes: 128-byte-wide box j at
+// j * (box bytes), K row kr at kr * 128, 16-byte chunk c of it at c ^ (kr mod 8).
+template <int ESZ>
 __device__ __forceinline__ void copy_b_elements(uint32_t dst, const Params& p, int k0, int n0, int ncols, int lane) {
-    const int chunks = ncols / 8;  // 16-byte chunks per K row
+    using G = Geom<ESZ>;
+    constexpr int EPW = 4 / ESZ;
+    constexpr int EPC = 16 / ESZ;
+    const int chunks = ncols / EPC;  // 16-byte chunks per K row
 #pragma unroll 1
-    for (int c = lane; c < BK * chunks; c += 32) {
+    for (int c = lane; c < G::KB * chunks; c += 32) {
         const int kr = c / chunks, cc = c - kr * chunks;
         const int j = cc >> 3, ch = cc & 7;
         const int k = k0 + kr;
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int n = n0 + cc * 8 + 2 * e;
-            const uint16_t* src = p.B + static_cast<int64_t>(k) * p.ldb + n;
-            const uint32_t lo = (k < p.K && n < p.N) ? __ldg(src) : 0u;
-            const uint32_t hi = (k < p.K && n + 1 < p.N) ? __ldg(src + 1) : 0u;
-            w[e] = lo | (hi << 16);
+            uint32_t word = 0;
+#pragma unroll
+            for (int t = 0; t < EPW; ++t) {
+                const int n = n0 + cc * EPC + e * EPW + t;
+                if (k < p.K && n < p.N)
+                    word |= load_elem<ESZ>(p.B, static_cast<int64_t>(k) * p.ldb + n) << (8 * ESZ * t);
+            }
+            w[e] = word;
         }
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + j * B_CHUNK_BYTES + kr * 128 +
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + j * G::B_BOX_BYTES + kr * 128 +
                                                                      ((ch ^ (kr & 7)) << 4)),
                      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                      : "memory");
@@ -330,8 +366,10 @@ __device__ __forceinline__ void add_bias(float (&v)[COLS], const float* __restri
 }
 
 // RES: the kernel adds a residual R (C = epilogue(A . B + R)); a separate
-// instantiation, so the plain epilogue carries none of its work.
-template <int BN, int OUT, int MODE, bool RES>
+// instantiation, so the plain epilogue carries none of its work.  ESZ: the
+// operands' element size, 2 (fp16 / bf16, kind::f16) or 1 (FP8 E4M3,
+// kind::f8f6f4).
+template <int BN, int OUT, int MODE, bool RES, int ESZ>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
@@ -342,6 +380,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int CG = PAIR ? 2 : 1;           // cta_group of every tcgen05 instruction
     constexpr int BL = PAIR ? BN / 2 : BN;     // B columns staged by this CTA
     using L = Layout<BN, BL>;
+    using G = Geom<ESZ>;
+    static_assert(BL % G::BOXC == 0, "B is staged in whole 128-byte-wide boxes");
     static_assert((BL / 64) % (MODE == 2 ? 2 : 1) == 0, "each CTA of a cluster copies whole B boxes");
     constexpr uint16_t CLUSTER_MASK = static_cast<uint16_t>((1u << CM) - 1u);
     const uint32_t rank = (CM > 1) ? cluster_ctarank() : 0u;
@@ -433,18 +473,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t sa = base + slot * L::STAGE_BYTES;
                         if (lane == 0 && tx > 0) {
                             mbar_expect_tx(full_bar(slot), tx);
-                            if (p.a_tma) tma_load_2d(sa, &tmA, full_bar(slot), kc * BK, mb * BM);
+                            if (p.a_tma) tma_load_2d(sa, &tmA, full_bar(slot), kc * G::KB, mb * BM);
                             if (p.b_tma) {
 #pragma unroll
-                                for (int j = 0; j < BN / 64; ++j)
-                                    tma_load_2d(sa + A_STAGE_BYTES + j * B_CHUNK_BYTES, &tmB, full_bar(slot),
-                                                nb * BN + j * 64, kc * BK);
+                                for (int j = 0; j < BN / G::BOXC; ++j)
+                                    tma_load_2d(sa + A_STAGE_BYTES + j * G::B_BOX_BYTES, &tmB, full_bar(slot),
+                                                nb * BN + j * G::BOXC, kc * G::KB);
                             }
                             issued |= 1u << slot;
                             last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
                         }
-                        if (!p.a_tma) copy_a_elements(sa, p, mb * BM, kc * BK, lane);
-                        if (!p.b_tma) copy_b_elements(sa + A_STAGE_BYTES, p, kc * BK, nb * BN, BN, lane);
+                        if (!p.a_tma) copy_a_elements<ESZ>(sa, p, mb * BM, kc * G::KB, lane);
+                        if (!p.b_tma) copy_b_elements<ESZ>(sa + A_STAGE_BYTES, p, kc * G::KB, nb * BN, BN, lane);
                         // the MMA reads these bytes through the async proxy
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -483,22 +523,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             // both CTAs' copies complete on the even CTA's barrier
                             const uint32_t fb = mapa_shared(full_bar(slot), 0);
                             if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), 2 * L::STAGE_BYTES);
-                            tma_load_2d_pair(sa, &tmA, fb, kc * BK, mb * BM);
+                            tma_load_2d_pair(sa, &tmA, fb, kc * G::KB, mb * BM);
 #pragma unroll
-                            for (int j = 0; j < BL / 64; ++j)
-                                tma_load_2d_pair(sa + A_STAGE_BYTES + j * B_CHUNK_BYTES, &tmB, fb,
-                                                 nb * BN + static_cast<int>(rank) * BL + j * 64, kc * BK);
+                            for (int j = 0; j < BL / G::BOXC; ++j)
+                                tma_load_2d_pair(sa + A_STAGE_BYTES + j * G::B_BOX_BYTES, &tmB, fb,
+                                                 nb * BN + static_cast<int>(rank) * BL + j * G::BOXC, kc * G::KB);
                         } else {
                             mbar_arrive_expect_tx(full_bar(slot), L::STAGE_BYTES);
-                            tma_load_2d(sa, &tmA, full_bar(slot), kc * BK, mb * BM);
+                            tma_load_2d(sa, &tmA, full_bar(slot), kc * G::KB, mb * BM);
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j) {
-                                const uint32_t dst = sa + A_STAGE_BYTES + j * B_CHUNK_BYTES;
+                            for (int j = 0; j < BN / G::BOXC; ++j) {
+                                const uint32_t dst = sa + A_STAGE_BYTES + j * G::B_BOX_BYTES;
                                 if constexpr (MODE == 1) {
-                                    tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK);
+                                    tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC, kc * G::KB);
                                 } else if (j % 2 == static_cast<int>(rank)) {
-                                    tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * 64, kc * BK,
-                                                          CLUSTER_MASK);
+                                    tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC,
+                                                          kc * G::KB, CLUSTER_MASK);
                                 }
                             }
                         }
@@ -542,21 +582,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // A: K-major, 8-row groups 1024 B apart.  B: MN-major, 8-K-row
                     // groups 1024 B apart, 64-column blocks one TMA box apart.
                     const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
-                    const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE_BYTES, B_CHUNK_BYTES, 1024);
+                    const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE_BYTES, G::B_BOX_BYTES, 1024);
                     // K steps that lie wholly past K would only add products of
                     // zero-filled elements: skip them
-                    const int ksteps = min(BK / UMMA_K, (p.K - kc * BK + UMMA_K - 1) / UMMA_K);
+                    const int ksteps = min(G::KB / G::UK, (p.K - kc * G::KB + G::UK - 1) / G::UK);
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                    for (int k = 0; k < G::KB / G::UK; ++k) {
                         // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
                         if (k < ksteps) {
-                            const uint64_t ad = a_desc + ((k * UMMA_K * 2) >> 4);
-                            const uint64_t bd = b_desc + ((k * UMMA_K * 128) >> 4);
+                            const uint64_t ad = a_desc + ((k * 32) >> 4);  // +32 bytes of K along the row
+                            const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
                             const uint32_t acc = (kc | k) != 0 ? 1u : 0u;
                             if constexpr (PAIR) {
-                                umma_f16_pair(d_tmem, ad, bd, p.idesc, acc);
+                                umma_pair<ESZ>(d_tmem, ad, bd, p.idesc, acc);
                             } else {
-                                umma_f16(d_tmem, ad, bd, p.idesc, acc);
+                                umma<ESZ>(d_tmem, ad, bd, p.idesc, acc);
                             }
                         }
                     }

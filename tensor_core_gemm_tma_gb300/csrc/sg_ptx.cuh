@@ -222,6 +222,18 @@ __device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        "}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on the barrier at the same offset in each CTA of `mask` when the
 // pair's previously issued tcgen05 operations complete.
 __device__ __forceinline__ void umma_commit_pair_multicast(uint32_t bar, uint16_t mask) {
@@ -253,6 +265,20 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         " .reg .pred p;\n"
         " setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The same with 8-bit operands (kind::f8f6f4; E4M3 by the instruction
+// descriptor), fp32 accumulate.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
         "}\n"
         ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
@@ -322,6 +348,25 @@ __device__ __forceinline__ uint32_t cvt_relu_bf16x2(float lo, float hi) {
     return d;
 }
 
+// The MMA for the operands' element size (2: kind::f16, 1: kind::f8f6f4).
+template <int ESZ>
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (ESZ == 2) {
+        umma_f16(d, a, b, idesc, acc);
+    } else {
+        umma_f8(d, a, b, idesc, acc);
+    }
+}
+
+template <int ESZ>
+__device__ __forceinline__ void umma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (ESZ == 2) {
+        umma_f16_pair(d, a, b, idesc, acc);
+    } else {
+        umma_f8_pair(d, a, b, idesc, acc);
+    }
+}
+
 // --------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor (tcgen05 format, version 1) for a tile
@@ -336,6 +381,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= 1ull << 46;  // descriptor version for tcgen05
     d |= 2ull << 61;  // SWIZZLE_128B
     return d;
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format 0) and
+// an fp32 accumulator; the field layout is that of kind::f16.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n, bool b_mn_major) {
+    return (1u << 4)                                   // D format: F32
+           | (0u << 7) | (0u << 10)                    // A, B format: E4M3
+           | ((b_mn_major ? 1u : 0u) << 16)            // B major: MN
+           | (static_cast<uint32_t>(n >> 3) << 17)
+           | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 // Instruction descriptor for kind::f16 with an fp32 accumulator:

@@ -14,11 +14,12 @@ TORCH_DT = None
 
 def torch_dtype(name):
     import torch
-    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[name]
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+            "e4m3": torch.float8_e4m3fn}[name]
 
 
 def bits_dtype(name):
-    return np.uint32 if name == "f32" else np.uint16
+    return {"f32": np.uint32, "e4m3": np.uint8}.get(name, np.uint16)
 
 
 def decode_np(bits: np.ndarray, name: str) -> np.ndarray:
@@ -36,6 +37,8 @@ def to_device_bits(bits: np.ndarray, name: str, device):
     import torch
     if name == "f32":
         t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int32))
+    elif name == "e4m3":
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.uint8))
     else:
         t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
     return t.to(device).view(torch_dtype(name))
@@ -90,7 +93,7 @@ def compare(got_bits: np.ndarray, ref_bits: np.ndarray, S: np.ndarray, out_dt: s
     return float(err.max()) if err.size else 0.0
 
 
-NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0, "e4m3": 0x7F}
 
 
 def seeded_case(M, N, K, in_dt, seed, dist=("normal", 0.0, 1.0), lda=None, ldb=None, pad_bits=None):
@@ -100,11 +103,11 @@ def seeded_case(M, N, K, in_dt, seed, dist=("normal", 0.0, 1.0), lda=None, ldb=N
     a = gemm_inputs.matrix_bits(seed, 0, M, K, dist, in_dt)
     b = gemm_inputs.matrix_bits(seed, 1, K, N, dist, in_dt)
     if lda is not None and lda > K:
-        ap = np.full((M, lda), pad_bits, np.uint16)
+        ap = np.full((M, lda), pad_bits, a.dtype)
         ap[:, :K] = a
         a = ap
     if ldb is not None and ldb > N:
-        bp = np.full((K, ldb), pad_bits, np.uint16)
+        bp = np.full((K, ldb), pad_bits, b.dtype)
         bp[:, :N] = b
         b = bp
     return a, b
