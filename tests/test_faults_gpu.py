@@ -1,7 +1,8 @@
 """Failure detection without a GPU fault: a copy that never happens makes
 the MMA issuer's bounded wait run out; the kernel records the timeout,
-every role drains its own work and exits, the host reads SG_ERR_TIMEOUT,
-and the context stays usable for the next, correct call."""
+every role drains its own work and exits (in the cluster modes both CTAs
+of a pair meet at the final cluster barrier), the host reads
+SG_ERR_TIMEOUT, and the context stays usable for the next, correct call."""
 import numpy as np
 import pytest
 
@@ -11,26 +12,33 @@ from parity_util import compare, run_gpu, seeded_case
 pytestmark = pytest.mark.gpu
 
 
-def test_skipped_copy_times_out_and_context_survives():
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_skipped_copy_times_out_and_context_survives(mode):
     import torch
     from tensor_core_gemm_tma_gb300 import _build
     _build.build()
     import tensor_core_gemm_tma_gb300 as sg
     lib = sg.load_library()
-    M, N, K = 512, 512, 512
+    M, N, K = 1024, 512, 512
     a, b = seeded_case(M, N, K, "f16", seed=31)
     A = torch.from_numpy(a.view(np.int16)).cuda().view(torch.float16)
     B = torch.from_numpy(b.view(np.int16)).cuda().view(torch.float16)
     old = sg.get_wait_limit_ns()
     try:
+        assert lib.sg_test_set_cluster(mode) == 0
+        assert lib.sg_test_set_tile_n(256) == 0
+        p = sg.plan(M, N, K, torch.float16, torch.float32)
+        assert p["cluster_m"] == (1 if mode == 1 else 2) and p["pair_mma"] == (1 if mode == 3 else 0)
         sg.set_wait_limit_ns(50_000_000)          # 50 ms
         lib.sg_test_set_skip_load(1)
-        C = sg.stage_gemm(A, B)                   # the launch itself succeeds
+        sg.stage_gemm(A, B)                       # the launch itself succeeds
         assert sg.device_status() == -8           # SG_ERR_TIMEOUT, reported asynchronously
         assert sg.device_status() == 0            # the record is cleared once read
     finally:
         lib.sg_test_set_skip_load(-1)
         sg.set_wait_limit_ns(old)
+        lib.sg_test_set_cluster(0)
+        lib.sg_test_set_tile_n(0)
     got = run_gpu(a, b, M, N, K, "f16", "f32")
     ref, _, S = oracle.gemm(a, b, "f16", "f32")
-    compare(got, ref, S, "f32", "after-timeout")
+    compare(got, ref, S, "f32", f"after-timeout mode {mode}")
