@@ -41,8 +41,8 @@ struct DevState {
     int major = 0, minor = 0;
     int* status = nullptr;  // device status word (4 bytes, library-owned)
     // per kernel instantiation [tile width][output type][mode - 1][residual]:
-    bool attr_done[2][3][3][3][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
-    int max_clusters[2][3][3][3][2] = {};  // the same index: co-resident clusters (0: not queried)
+    bool attr_done[2][3][3][4][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
+    int max_clusters[2][3][3][4][2] = {};  // the same index: co-resident clusters (0: not queried)
 };
 
 std::mutex g_mu;
@@ -183,6 +183,14 @@ struct Plan {
     int a_tma = 1, b_tma = 1;  // operand copied by TMA (1) or by element loads (0)
 };
 
+// Mode 4's shared memory: the resident B (k_chunks x n_blocks blocks of
+// bn columns by 128 bytes of K), a ring of A tiles (k_chunks chunks each),
+// the staging buffers and the barriers.
+int64_t smem_panel(int bn, int stages, int64_t k_chunks, int64_t n_blocks) {
+    return k_chunks * n_blocks * bn * sg::BK_BYTES + stages * k_chunks * sg::A_STAGE_BYTES +
+           sg::EPI_WARPS * sg::EPI_BUF_BYTES + sg::BAR_AREA + sg::SMEM_ALIGN;
+}
+
 int smem_for(int bn, int stages, int mode) {
     if (mode == 3) {  // each CTA stages half of B
         switch (bn) {
@@ -212,11 +220,11 @@ int forced_bn() { return g_force_bn.load(); }
 
 // Kernel mode forced by sg_test_set_cluster or, at load, the environment
 // variable STAGE_GEMM_CLUSTER (1: single CTA, 2: CTA pairs sharing B by
-// multicast, 3: paired MMA; 0: the planner's choice).
+// multicast, 3: paired MMA, 4: resident B; 0: the planner's choice).
 std::atomic<int> g_force_mode{[] {
     const char* e = std::getenv("STAGE_GEMM_CLUSTER");
     const int x = e ? std::atoi(e) : 0;
-    return (x >= 1 && x <= 3) ? x : 0;
+    return (x >= 1 && x <= 4) ? x : 0;
 }()};
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, const void* C,
@@ -253,26 +261,47 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // problem is large and the K loop long enough for operand traffic to
     // matter: each SM then stages only its half of B.
     const bool pairable = (bn / boxc) % 2 == 0;  // each CTA of a pair owns whole boxes of B
+    // Pairs of CTAs compute 256-row tiles with the paired MMA when the
+    // problem is large and the K loop long enough for operand traffic to
+    // matter: each SM then stages only its half of B.
     int mode = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pl->m_blocks * pl->n_blocks >= st.sm_count && pairable)
                    ? 3
                    : 1;
-    if (const int f = g_force_mode.load(); f == 1 || (f >= 2 && pairable)) mode = f;
-    if (choice && choice->mode && (choice->mode == 1 || pairable)) mode = choice->mode;
+    // Mode 4 (resident B) when B is small: at most 2 K chunks and 4 column
+    // blocks of 128, so all of B fits next to a ring of at least 2 A tiles,
+    // and there are enough row tiles to keep every SM busy.
+    const int64_t nb128 = cdiv(N, 128);
+    const bool panel_ok = a_tma && b_tma && pl->k_chunks <= 2 && nb128 <= 4 &&
+                          smem_panel(128, 2, pl->k_chunks, nb128) <= st.smem_optin;
+    if (panel_ok && pl->m_blocks >= st.sm_count && !forced_bn()) mode = 4;
+    auto legal = [&](int m) { return m == 1 || ((m == 2 || m == 3) && pairable) || (m == 4 && panel_ok); };
+    if (const int f = g_force_mode.load(); f && legal(f)) mode = f;
+    if (choice && choice->mode && legal(choice->mode)) mode = choice->mode;
     if (!a_tma || !b_tma) mode = 1;  // element-load staging runs in single-CTA mode
+    if (mode == 4) {
+        bn = 128;
+        pl->bn = bn;
+        pl->n_blocks = nb128;
+    }
     pl->mode = mode;
-    pl->cm = mode == 1 ? 1 : 2;
+    pl->cm = (mode == 2 || mode == 3) ? 2 : 1;
     const int cm = pl->cm;
-    pl->tiles = cdiv(pl->m_blocks, cm) * pl->n_blocks;  // cluster tiles
+    // work units handed out by the persistent loop: cluster tiles (modes 1-3)
+    // or row tiles covering every column block (mode 4)
+    pl->tiles = mode == 4 ? pl->m_blocks : cdiv(pl->m_blocks, cm) * pl->n_blocks;
     int maxs = 0;
-    for (int s = 1; s <= SG_MAX_STAGES; ++s)
-        if (smem_for(bn, s, mode) <= st.smem_optin) maxs = s;
+    for (int s = 1; s <= SG_MAX_STAGES; ++s) {
+        const int64_t need = mode == 4 ? smem_panel(bn, s, pl->k_chunks, pl->n_blocks) : smem_for(bn, s, mode);
+        if (need <= st.smem_optin) maxs = s;
+    }
     pl->max_stages = maxs;
     if (maxs == 0) return SG_ERR_STAGES;
     if (stages == 0 && choice && choice->stages) stages = std::min(choice->stages, maxs);
     if (stages == 0) stages = maxs;
     if (stages > maxs) return SG_ERR_STAGES;
     pl->stages = stages;
-    pl->smem = smem_for(bn, stages, mode);
+    pl->smem = mode == 4 ? static_cast<int>(smem_panel(bn, stages, pl->k_chunks, pl->n_blocks))
+                         : smem_for(bn, stages, mode);
     pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for
     // it; keep one persistent CTA per SM by asking for more than half of the
@@ -315,7 +344,9 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
                 const CUtensorMap& tc, const CUtensorMap& tr, const sg::Params& prm, bool residual,
                 cudaStream_t stream) {
     sg::LaunchFn fn = nullptr;
-    if (pl.block_k == sg::BK_BYTES)  // 8-bit operands
+    if (pl.mode == 4)
+        fn = sg::launcher_panel(out_dtype, residual, pl.block_k == sg::BK_BYTES ? 1 : 2);
+    else if (pl.block_k == sg::BK_BYTES)  // 8-bit operands
         fn = residual ? sg::launcher_fp8_res(pl.bn, out_dtype, pl.mode) : sg::launcher_fp8_plain(pl.bn, out_dtype, pl.mode);
     else if (pl.mode == 1)
         fn = residual ? sg::launcher_res_single(pl.bn, out_dtype) : sg::launcher_plain_single(pl.bn, out_dtype);
@@ -536,6 +567,12 @@ int sg_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
                 cands.push_back(c);
             }
         }
+        if (bn == 128 && a_tma && b_tma) {  // resident B, when it fits (the planner checks)
+            Choice c;
+            c.bn = 128;
+            c.mode = 4;
+            cands.push_back(c);
+        }
     }
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return SG_ERR_CUDA;
@@ -644,7 +681,7 @@ int sg_test_set_tile_n(int bn) {
 }
 
 int sg_test_set_cluster(int mode) {
-    if (mode < 0 || mode > 3) return SG_ERR_ARG;
+    if (mode < 0 || mode > 4) return SG_ERR_ARG;
     g_force_mode.store(mode);
     return SG_OK;
 }

@@ -31,6 +31,12 @@
 //      boxes and multicasts them into both CTAs' rings, halving the B
 //      traffic from L2; a ring slot is free only when both CTAs' MMAs have
 //      read it (the empty barrier counts one commit from each CTA).
+//   4  resident B ("decoded panels", Tolk.Stage): for a small K x N, each
+//      CTA stages all of B once (every K chunk of every 128-column block)
+//      and streams only A, one 128-row tile per ring slot; the MMAs of
+//      every column block of that row tile read the one A slot, each into
+//      its own rotating accumulator.  Tile units are (row tile, column
+//      block) in that order; the epilogue is the same as mode 1's.
 //   3  paired MMA (tcgen05 cta_group::2): the two CTAs of a cluster compute
 //      one 256 x BN tile.  Each CTA stages its own 128 rows of A and its own
 //      BN/2 columns of B (so a stage is 32 KiB instead of 48 KiB for
@@ -374,8 +380,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const Params p) {
-    static_assert(MODE >= 1 && MODE <= 3, "mode 1, 2 or 3");
-    constexpr int CM = (MODE == 1) ? 1 : 2;    // CTAs per cluster
+    static_assert(MODE >= 1 && MODE <= 4, "mode 1, 2, 3 or 4");
+    constexpr int CM = (MODE == 2 || MODE == 3) ? 2 : 1;  // CTAs per cluster
+    constexpr bool PANEL = (MODE == 4);        // B resident in shared memory
     constexpr bool PAIR = (MODE == 3);         // paired MMA (cta_group::2)
     constexpr int CG = PAIR ? 2 : 1;           // cta_group of every tcgen05 instruction
     constexpr int BL = PAIR ? BN / 2 : BN;     // B columns staged by this CTA
@@ -396,8 +403,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t base = (raw + SMEM_ALIGN - 1) & ~static_cast<uint32_t>(SMEM_ALIGN - 1);
     uint8_t* gbase = smem_raw + (base - raw);
     const int stages = p.stages;
+    // Shared-memory map.  Modes 1-3: [ring][staging][barriers].  Mode 4:
+    // [resident B: k_chunks x n_blocks blocks of BN columns][ring of A tiles,
+    // each k_chunks A chunks][staging][barriers].
+    constexpr int B_BLOCK_BYTES = (BN / G::BOXC) * G::B_BOX_BYTES;  // one K chunk of one column block
+    const uint32_t res_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks * p.n_blocks) * B_BLOCK_BYTES : 0u;
+    const uint32_t stage_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks) * A_STAGE_BYTES : L::STAGE_BYTES;
+    const uint32_t ring0 = base + res_bytes;
+    const uint32_t epi_off = res_bytes + static_cast<uint32_t>(stages) * stage_bytes;
+    const uint32_t bar_off = epi_off + EPI_WARPS * EPI_BUF_BYTES;
 
-    const uint32_t bar0 = base + L::bar_offset(stages);
+    const uint32_t bar0 = base + bar_off;
     // barrier slots: full[0..7], empty[8..15], tmem_full[16..19], tmem_empty[20..23], drain[24],
     // then the tensor-memory address and abort flag, then residual[0..7] at 32..39
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -405,10 +421,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * SG_MAX_STAGES + MAX_ACC + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * SG_MAX_STAGES + 2 * MAX_ACC);
-    uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(gbase + L::bar_offset(stages) + 8 * (2 * SG_MAX_STAGES + 2 * MAX_ACC + 1));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + bar_off + 8 * (2 * SG_MAX_STAGES + 2 * MAX_ACC + 1));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     auto rres_bar = [&](int e) { return bar0 + 8u * (32 + e); };  // residual tile landed (one per epilogue warp)
+    const uint32_t bres_bar = bar0 + 8u * 40;                      // mode 4: the resident B has landed
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -424,6 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(drain_bar, 1);
         for (int e = 0; e < EPI_WARPS; ++e) mbar_init(rres_bar(e), 1);
+        mbar_init(bres_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -470,7 +487,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     if (it != p.skip_load) {
-                        const uint32_t sa = base + slot * L::STAGE_BYTES;
+                        const uint32_t sa = ring0 + slot * stage_bytes;
                         if (lane == 0 && tx > 0) {
                             mbar_expect_tx(full_bar(slot), tx);
                             if (p.a_tma) tma_load_2d(sa, &tmA, full_bar(slot), kc * G::KB, mb * BM);
@@ -508,18 +525,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued = 0, last_parity = 0;  // per slot: ever filled, parity of its last fill
             int64_t it = 0;
             bool ok = true;
+            if constexpr (PANEL) {
+                // the resident B: every K chunk of every column block, once
+                mbar_arrive_expect_tx(bres_bar, res_bytes);
+                for (int kc = 0; kc < p.k_chunks; ++kc)
+                    for (int nb = 0; nb < p.n_blocks; ++nb)
+#pragma unroll
+                        for (int j = 0; j < BN / G::BOXC; ++j)
+                            tma_load_2d(base + (kc * p.n_blocks + nb) * B_BLOCK_BYTES + j * G::B_BOX_BYTES, &tmB,
+                                        bres_bar, nb * BN + j * G::BOXC, kc * G::KB);
+            }
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
-                int mb, nb;
-                tile_coords<CM>(tile, p, rank, mb, nb);
-                for (int kc = 0; kc < p.k_chunks; ++kc, ++it) {
+                int mb = tile, nb = 0;
+                if constexpr (!PANEL) tile_coords<CM>(tile, p, rank, mb, nb);
+                const int fills = PANEL ? 1 : p.k_chunks;  // mode 4: one ring slot holds every K chunk of A
+                for (int kc = 0; kc < fills; ++kc, ++it) {
                     if (!wait_bounded(empty_bar(slot), phase ^ 1u, abort_flag, p.status, p.wait_limit_ns,
                                       SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
                     if (it != p.skip_load) {
-                        const uint32_t sa = base + slot * L::STAGE_BYTES;
-                        if constexpr (PAIR) {
+                        const uint32_t sa = ring0 + slot * stage_bytes;
+                        if constexpr (PANEL) {
+                            mbar_arrive_expect_tx(full_bar(slot), stage_bytes);
+                            for (int c = 0; c < p.k_chunks; ++c)
+                                tma_load_2d(sa + c * A_STAGE_BYTES, &tmA, full_bar(slot), c * G::KB, mb * BM);
+                        } else if constexpr (PAIR) {
                             // both CTAs' copies complete on the even CTA's barrier
                             const uint32_t fb = mapa_shared(full_bar(slot), 0);
                             if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), 2 * L::STAGE_BYTES);
@@ -556,6 +588,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // even CTA's barriers also count the odd CTA's copies)
                 for (int s = 0; s < stages; ++s)
                     if ((issued >> s) & 1u) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
+                if (PANEL) wait_drain(bres_bar, 0, p.wait_limit_ns);
             }
         }
     } else if (warp == 1) {
@@ -564,7 +597,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t slot = 0, phase = 0;
             uint32_t ab = 0, aph = 0;  // accumulator index and its phase
             bool ok = true;
+            if constexpr (PANEL) {
+                ok = wait_bounded(bres_bar, 0, abort_flag, p.status, p.wait_limit_ns, SITE_MMA_FULL);
+                if (ok) tc_fence_after();
+            }
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+                if constexpr (PANEL) {
+                    // one A slot, every column block of the resident B
+                    if (!wait_bounded(full_bar(slot), phase, abort_flag, p.status, p.wait_limit_ns, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = ring0 + slot * stage_bytes;
+                    for (int nb = 0; nb < p.n_blocks; ++nb) {
+                        if (!wait_bounded(tempty_bar(ab), aph ^ 1u, abort_flag, p.status, p.wait_limit_ns,
+                                          SITE_MMA_TMEM_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + ab * BN;
+                        for (int kc = 0; kc < p.k_chunks; ++kc) {
+                            const uint64_t a_desc = smem_desc_sw128(sa + kc * A_STAGE_BYTES, 16, 1024);
+                            const uint64_t b_desc = smem_desc_sw128(base + (kc * p.n_blocks + nb) * B_BLOCK_BYTES,
+                                                                    G::B_BOX_BYTES, 1024);
+                            const int ksteps = min(G::KB / G::UK, (p.K - kc * G::KB + G::UK - 1) / G::UK);
+#pragma unroll
+                            for (int k = 0; k < G::KB / G::UK; ++k) {
+                                if (k < ksteps)
+                                    umma<ESZ>(d_tmem, a_desc + ((k * 32) >> 4), b_desc + ((k * G::B_KSTEP_BYTES) >> 4),
+                                              p.idesc, (kc | k) != 0 ? 1u : 0u);
+                            }
+                        }
+                        umma_commit(tfull_bar(ab));
+                        if (++ab == static_cast<uint32_t>(ACC)) {
+                            ab = 0;
+                            aph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(empty_bar(slot));  // the A slot is free once every block has read it
+                    if (++slot == static_cast<uint32_t>(stages)) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                    continue;
+                }
                 if (!wait_bounded(tempty_bar(ab), aph ^ 1u, abort_flag, p.status, p.wait_limit_ns,
                                   SITE_MMA_TMEM_EMPTY)) {
                     ok = false;
@@ -578,7 +657,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + slot * L::STAGE_BYTES;
+                    const uint32_t sa = ring0 + slot * stage_bytes;
                     // A: K-major, 8-row groups 1024 B apart.  B: MN-major, 8-K-row
                     // groups 1024 B apart, 64-column blocks one TMA box apart.
                     const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
@@ -600,7 +679,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             }
                         }
                     }
-                    if constexpr (MODE == 1) {
+                    if constexpr (MODE == 1 || MODE == 4) {
                         umma_commit(empty_bar(slot));
                     } else if constexpr (MODE == 2) {
                         umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slot in both CTAs
@@ -637,7 +716,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;                   // the tensor-memory lane quarter this warp may read
         constexpr int SPLIT = EPI_WARPS / 4;      // warps sharing a quarter
         const int part = e / 4;                   // which of them: takes column chunks part, part+SPLIT, ...
-        const uint32_t buf = base + L::epi_offset(stages) + e * EPI_BUF_BYTES;
+        const uint32_t buf = base + epi_off + e * EPI_BUF_BYTES;
         const bool r_staged = RES && p.r_tma;  // residual tiles arrive by TMA in the staging buffer
         uint32_t r_phase = 0;
         bool r_pending = false;                    // a residual load is in flight into `buf`
@@ -652,9 +731,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             r_pending = true;
         };
         uint32_t ab = 0, aph = 0;
-        for (int tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
-            int mb, nb;
-            tile_coords<CM>(tile, p, rank, mb, nb);
+        // units: one per tile (modes 1-3), or (row tile, column block) pairs (mode 4)
+        const int subs = PANEL ? p.n_blocks : 1;
+        for (int tile = cluster_id, sub = 0; tile < p.num_tiles;) {
+            int mb = tile, nb = sub;
+            if constexpr (!PANEL) tile_coords<CM>(tile, p, rank, mb, nb);
             const int row0 = mb * BM + q * 32;
             const int row = row0 + lane;
             // the residual of this warp's first chunk loads while the MMAs run
@@ -776,6 +857,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (++ab == static_cast<uint32_t>(ACC)) {
                 ab = 0;
                 aph ^= 1u;
+            }
+            if (++sub == subs) {
+                sub = 0;
+                tile += num_clusters;
             }
         }
         // leaving early with a residual load in flight: let it land first

@@ -35,7 +35,7 @@ using LaunchFn = int (*)(LaunchArgs&);
 
 template <int BN, int OUT, int MODE, bool RES, int ESZ>
 int launch_kernel(LaunchArgs& a) {
-    constexpr int CM = MODE == 1 ? 1 : 2;
+    constexpr int CM = (MODE == 2 || MODE == 3) ? 2 : 1;  // CTAs per cluster
     auto kern = sg_gemm_kernel<BN, OUT, MODE, RES, ESZ>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -85,5 +85,7 @@ LaunchFn launcher_res_pair(int bn, int out, int mode);
 // FP8 E4M3 operands (tile widths 128 and 256; pairs only at 256):
 LaunchFn launcher_fp8_plain(int bn, int out, int mode);
 LaunchFn launcher_fp8_res(int bn, int out, int mode);
+// Mode 4 (resident B), tile width 128, either element size (esz 1 or 2):
+LaunchFn launcher_panel(int out, bool residual, int esz);
 
 }  // namespace sg
