@@ -260,8 +260,8 @@ def config_of(w, plan):
         c["tile"] = f"{rows}x{plan['block_n']}x{plan['block_k']}"
         c["stages"] = plan["stages"]
         c["grid"] = plan["grid"]
-        c["kernel_mode"] = ("paired MMA (cta_group::2)" if plan.get("pair_mma") else
-                            "CTA pair, B multicast" if plan.get("cluster_m") == 2 else "single CTA")
+        c["kernel_mode"] = {1: "single CTA", 2: "CTA pair, B multicast", 3: "paired MMA (cta_group::2)",
+                            4: "resident B (one CTA per row tile, all of B in shared memory)"}.get(plan.get("mode"))
         c["raster_group_m"] = plan.get("group_m")
         c["tuned"] = plan.get("tuned", False)
     return c
@@ -347,6 +347,36 @@ def whole_job_tflops(flops_per_step: float, world: int, steps: int, max_sum_ms: 
     """Every rank runs the same workload (replicas): total FLOPs of all
     ranks over the slowest rank's summed step time."""
     return flops_per_step * world * steps / (max_sum_ms * 1e-3) / 1e12
+
+
+def dram_reference(device, nbytes_write: int, steps: int = 10):
+    """Same-run DRAM references for an HBM-bound workload: a device memset
+    of the workload's output bytes (write only) and a device-to-device copy
+    of as many bytes (read + write), each timed like the GEMM (L2 flushed
+    before each step, CUDA events).  Returns GB/s figures."""
+    import torch
+    n = (nbytes_write + 1) // 2
+    x = torch.empty(n, dtype=torch.float16, device=device)
+    y = torch.empty(n, dtype=torch.float16, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def med(fn):
+        for _ in range(2):
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+    w_ms = med(lambda: x.zero_())
+    c_ms = med(lambda: y.copy_(x))
+    return {"write_only_gbs": 2 * n / (w_ms * 1e-3) / 1e9, "copy_gbs": 4 * n / (c_ms * 1e-3) / 1e9,
+            "bytes": 2 * n, "how": "cudaMemsetAsync of the output's bytes; device copy of as many bytes (read+write)"}
 
 
 def roofline_of(w, ms, peaks, traffic):
@@ -436,6 +466,8 @@ def main():
     }
     if w.name in HBM_BOUND:
         line["hbm_gbs"] = line["roofline"]["achieved"]
+        out_bytes = w.M * w.N * {"f32": 4, "f16": 2, "bf16": 2}[w.out_dtype]
+        line["dram_reference"] = dram_reference(device, out_bytes)
 
     if rank == 0 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD:
         sec = []

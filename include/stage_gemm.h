@@ -170,7 +170,9 @@ typedef struct {
                               (with cluster_m 2: the pair shares each B tile by
                               multicast) */
     int32_t group_m;       /* cluster row blocks swept together by the tile raster */
-    int32_t reserved[2];
+    int32_t mode;          /* 1 single CTA, 2 CTA pair sharing B by multicast,
+                              3 paired MMA, 4 B resident in shared memory */
+    int32_t reserved[1];
 } sg_plan_info;
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,

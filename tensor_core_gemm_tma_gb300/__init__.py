@@ -44,7 +44,7 @@ class SgError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "block_n", "block_k", "stages", "max_stages", "tiles", "grid", "threads", "smem_bytes",
-        "tmem_columns", "tma_store", "cluster_m", "pair_mma", "group_m")] + [("reserved", ctypes.c_int32 * 2)]
+        "tmem_columns", "tma_store", "cluster_m", "pair_mma", "group_m", "mode")] + [("reserved", ctypes.c_int32 * 1)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}

@@ -390,6 +390,7 @@ void fill_info(const Plan& pl, sg_plan_info* info) {
     info->cluster_m = pl.cm;
     info->pair_mma = pl.mode == 3 ? 1 : 0;
     info->group_m = pl.group_m;
+    info->mode = pl.mode;
 }
 
 bool c_tma_legal(const void* C, int64_t M, int64_t ldc, int out_dtype) {

@@ -43,7 +43,7 @@ def test_panel_bit_identical_to_single_cta(M, N, K, out_dt):
     a, b = seeded_case(M, N, K, "f16", seed=M + N + K, lda=(K + 7) // 8 * 8, ldb=(N + 7) // 8 * 8)
     bias = np.linspace(-1, 1, N).astype(np.float32)
     p4 = _forced(4, lambda: _plan(M, N, K, "f16", out_dt))
-    assert p4["block_n"] == 128 and p4["tiles"] == (M + 127) // 128
+    assert p4["block_n"] == 128 and p4["tiles"] == (M + 127) // 128 and p4["mode"] == 4
     got4 = _forced(4, lambda: run_gpu(a, b, M, N, K, "f16", out_dt, "bias_relu", bias))
     got1 = _forced(1, lambda: run_gpu(a, b, M, N, K, "f16", out_dt, "bias_relu", bias))
     assert np.array_equal(got4, got1)
@@ -83,4 +83,4 @@ def test_panel_fp8():
 
 def test_panel_is_the_default_for_the_skinny_projection():
     p = _plan(518400, 384, 96, "f16", "f16")
-    assert p["tiles"] == 4050 and p["block_n"] == 128 and p["cluster_m"] == 1 and p["pair_mma"] == 0
+    assert p["tiles"] == 4050 and p["block_n"] == 128 and p["mode"] == 4
