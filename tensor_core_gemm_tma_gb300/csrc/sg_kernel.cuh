@@ -258,6 +258,19 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
     }
 }
 
+// The same wait with its first polls inline, for the MMA issuer: it waits
+// once per K chunk, and a call on that path showed up as idle tensor-pipe
+// cycles.  After INLINE_POLLS failed polls it continues in wait_bounded, whose
+// time limit then applies.
+constexpr int INLINE_POLLS = 64;
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          uint64_t limit, int site) {
+#pragma unroll 1
+    for (int i = 0; i < INLINE_POLLS; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded(bar, parity, abort_flag, status, limit, site);
+}
+
 // Bounded wait that ignores the abort flag: used to drain a role's own
 // asynchronous work before the CTA exits.
 static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
@@ -593,66 +606,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0 && p.k_chunks > 0 && (!PAIR || rank == 0)) {
+        // The whole warp runs the loop, so slots, phases and descriptors stay
+        // warp-uniform; lane 0 issues each tcgen05 instruction.
+        if (p.k_chunks > 0 && (!PAIR || rank == 0)) {
+            const bool issuer = lane == 0;
+            auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
+                return __all_sync(0xffffffffu, wait_fast(bar, parity, abort_flag, p.status, p.wait_limit_ns, site));
+            };
             uint32_t slot = 0, phase = 0;
             uint32_t ab = 0, aph = 0;  // accumulator index and its phase
             bool ok = true;
             if constexpr (PANEL) {
-                ok = wait_bounded(bres_bar, 0, abort_flag, p.status, p.wait_limit_ns, SITE_MMA_FULL);
+                ok = wait_all(bres_bar, 0, SITE_MMA_FULL);
                 if (ok) tc_fence_after();
             }
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 if constexpr (PANEL) {
                     // one A slot, every column block of the resident B
-                    if (!wait_bounded(full_bar(slot), phase, abort_flag, p.status, p.wait_limit_ns, SITE_MMA_FULL)) {
+                    if (!wait_all(full_bar(slot), phase, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sa = ring0 + slot * stage_bytes;
                     for (int nb = 0; nb < p.n_blocks; ++nb) {
-                        if (!wait_bounded(tempty_bar(ab), aph ^ 1u, abort_flag, p.status, p.wait_limit_ns,
-                                          SITE_MMA_TMEM_EMPTY)) {
+                        if (!wait_all(tempty_bar(ab), aph ^ 1u, SITE_MMA_TMEM_EMPTY)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint32_t d_tmem = tmem_base + ab * BN;
-                        for (int kc = 0; kc < p.k_chunks; ++kc) {
-                            const uint64_t a_desc = smem_desc_sw128(sa + kc * A_STAGE_BYTES, 16, 1024);
-                            const uint64_t b_desc = smem_desc_sw128(base + (kc * p.n_blocks + nb) * B_BLOCK_BYTES,
-                                                                    G::B_BOX_BYTES, 1024);
-                            const int ksteps = min(G::KB / G::UK, (p.K - kc * G::KB + G::UK - 1) / G::UK);
+                        if (issuer) {
+                            for (int kc = 0; kc < p.k_chunks; ++kc) {
+                                const uint64_t a_desc = smem_desc_sw128(sa + kc * A_STAGE_BYTES, 16, 1024);
+                                const uint64_t b_desc = smem_desc_sw128(
+                                    base + (kc * p.n_blocks + nb) * B_BLOCK_BYTES, G::B_BOX_BYTES, 1024);
+                                const int ksteps = min(G::KB / G::UK, (p.K - kc * G::KB + G::UK - 1) / G::UK);
 #pragma unroll
-                            for (int k = 0; k < G::KB / G::UK; ++k) {
-                                if (k < ksteps)
-                                    umma<ESZ>(d_tmem, a_desc + ((k * 32) >> 4), b_desc + ((k * G::B_KSTEP_BYTES) >> 4),
-                                              p.idesc, (kc | k) != 0 ? 1u : 0u);
+                                for (int k = 0; k < G::KB / G::UK; ++k) {
+                                    if (k < ksteps)
+                                        umma<ESZ>(d_tmem, a_desc + ((k * 32) >> 4),
+                                                  b_desc + ((k * G::B_KSTEP_BYTES) >> 4), p.idesc,
+                                                  (kc | k) != 0 ? 1u : 0u);
+                                }
                             }
+                            umma_commit(tfull_bar(ab));
                         }
-                        umma_commit(tfull_bar(ab));
                         if (++ab == static_cast<uint32_t>(ACC)) {
                             ab = 0;
                             aph ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    umma_commit(empty_bar(slot));  // the A slot is free once every block has read it
+                    if (issuer) umma_commit(empty_bar(slot));  // the A slot is free once every block has read it
                     if (++slot == static_cast<uint32_t>(stages)) {
                         slot = 0;
                         phase ^= 1u;
                     }
                     continue;
                 }
-                if (!wait_bounded(tempty_bar(ab), aph ^ 1u, abort_flag, p.status, p.wait_limit_ns,
-                                  SITE_MMA_TMEM_EMPTY)) {
+                if (!wait_all(tempty_bar(ab), aph ^ 1u, SITE_MMA_TMEM_EMPTY)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * BN;
                 for (int kc = 0; kc < p.k_chunks; ++kc) {
-                    if (!wait_bounded(full_bar(slot), phase, abort_flag, p.status, p.wait_limit_ns, SITE_MMA_FULL)) {
+                    if (!wait_all(full_bar(slot), phase, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -665,26 +685,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // K steps that lie wholly past K would only add products of
                     // zero-filled elements: skip them
                     const int ksteps = min(G::KB / G::UK, (p.K - kc * G::KB + G::UK - 1) / G::UK);
+                    if (issuer) {
 #pragma unroll
-                    for (int k = 0; k < G::KB / G::UK; ++k) {
-                        // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
-                        if (k < ksteps) {
-                            const uint64_t ad = a_desc + ((k * 32) >> 4);  // +32 bytes of K along the row
-                            const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
-                            const uint32_t acc = (kc | k) != 0 ? 1u : 0u;
-                            if constexpr (PAIR) {
-                                umma_pair<ESZ>(d_tmem, ad, bd, p.idesc, acc);
-                            } else {
-                                umma<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                        for (int k = 0; k < G::KB / G::UK; ++k) {
+                            // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
+                            if (k < ksteps) {
+                                const uint64_t ad = a_desc + ((k * 32) >> 4);  // +32 bytes of K along the row
+                                const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
+                                const uint32_t acc = (kc | k) != 0 ? 1u : 0u;
+                                if constexpr (PAIR) {
+                                    umma_pair<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                                } else {
+                                    umma<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                                }
                             }
                         }
-                    }
-                    if constexpr (MODE == 1 || MODE == 4) {
-                        umma_commit(empty_bar(slot));
-                    } else if constexpr (MODE == 2) {
-                        umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slot in both CTAs
-                    } else {
-                        umma_commit_pair_multicast(empty_bar(slot), CLUSTER_MASK);
+                        if constexpr (MODE == 1 || MODE == 4) {
+                            umma_commit(empty_bar(slot));
+                        } else if constexpr (MODE == 2) {
+                            umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slot in both CTAs
+                        } else {
+                            umma_commit_pair_multicast(empty_bar(slot), CLUSTER_MASK);
+                        }
                     }
                     if (++slot == static_cast<uint32_t>(stages)) {
                         slot = 0;
@@ -692,10 +714,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                if constexpr (PAIR) {
-                    umma_commit_pair_multicast(tfull_bar(ab), CLUSTER_MASK);  // both CTAs' epilogues
-                } else {
-                    umma_commit(tfull_bar(ab));
+                if (issuer) {
+                    if constexpr (PAIR) {
+                        umma_commit_pair_multicast(tfull_bar(ab), CLUSTER_MASK);  // both CTAs' epilogues
+                    } else {
+                        umma_commit(tfull_bar(ab));
+                    }
                 }
                 if (++ab == static_cast<uint32_t>(ACC)) {
                     ab = 0;
@@ -703,10 +727,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             // every MMA of this CTA has completed before tensor memory is released
-            if constexpr (PAIR) {
-                umma_commit_pair(drain_bar);
-            } else {
-                umma_commit(drain_bar);
+            if (issuer) {
+                if constexpr (PAIR) {
+                    umma_commit_pair(drain_bar);
+                } else {
+                    umma_commit(drain_bar);
+                }
             }
             wait_drain(drain_bar, 0, p.wait_limit_ns);
         }
