@@ -236,20 +236,26 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     pl->m_blocks = cdiv(M, sg::BM);
     pl->block_k = sg::BK_BYTES / esz;
     pl->k_chunks = cdiv(K, pl->block_k);
-    // Tile width: the widest of 256 / 192 / 128 that covers N as tightly as
-    // 128 does (no more padded columns) and still gives every SM a tile.  A
+    // Tile width: the one of 256 / 192 / 128 with the least estimated time,
+    // counted as whole waves of tiles over the SMs times the time of one tile
+    // (its width over its throughput relative to 256 columns).  Narrower tiles
+    // stage more operand bytes per product, and with every SM loading that
+    // costs throughput: 192 columns ran at ~0.78 and 128 at ~0.55 of 256 on
+    // GB300.  Those ratios are rough, so a narrower width must win by 5%.  A
     // short K loop (<= 4 chunks) makes the epilogue the bottleneck: keep 128,
     // whose four tensor-memory accumulators overlap it best.
     int bn = 128;
-    const double eff128 = static_cast<double>(N) / (cdiv(N, 128) * 128.0);
-    for (int cand : {256, 192}) {
-        if (cand % boxc) continue;
-        if (pl->k_chunks <= 4) break;
-        if (N < cand) continue;
-        const double eff = static_cast<double>(N) / (cdiv(N, cand) * static_cast<double>(cand));
-        if (pl->m_blocks * cdiv(N, cand) >= st.sm_count && eff >= eff128) {
-            bn = cand;
-            break;
+    if (pl->k_chunks > 4) {
+        double best = 0.0;
+        for (int cand : {256, 192, 128}) {
+            if (cand % boxc) continue;
+            const double rel = cand == 256 ? 1.0 : cand == 192 ? 0.78 : 0.55;
+            const int64_t waves = cdiv(pl->m_blocks * cdiv(N, cand), static_cast<int64_t>(st.sm_count));
+            const double cost = static_cast<double>(waves) * cand / rel;
+            if (best == 0.0 || cost < 0.95 * best) {
+                best = cost;
+                bn = cand;
+            }
         }
     }
     if (forced_bn()) bn = forced_bn();
@@ -257,16 +263,12 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     pl->bn = bn;
     pl->group_m = (choice && choice->group_m) ? choice->group_m : kGroupM;
     pl->n_blocks = cdiv(N, bn);
-    // Pairs of CTAs compute 256-row tiles with the paired MMA when the
-    // problem is large and the K loop long enough for operand traffic to
-    // matter: each SM then stages only its half of B.
     const bool pairable = (bn / boxc) % 2 == 0;  // each CTA of a pair owns whole boxes of B
-    // Pairs of CTAs compute 256-row tiles with the paired MMA when the
-    // problem is large and the K loop long enough for operand traffic to
-    // matter: each SM then stages only its half of B.
-    int mode = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pl->m_blocks * pl->n_blocks >= st.sm_count && pairable)
-                   ? 3
-                   : 1;
+    // Pairs of CTAs compute 256-row tiles with the paired MMA when the K loop
+    // is long enough for operand traffic to matter: each SM then stages only
+    // its half of B.  A pair tile is two SMs' work, so pairing keeps as many
+    // SMs busy as single-CTA tiles do.
+    int mode = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pairable) ? 3 : 1;
     // Mode 4 (resident B) when B is small: at most 2 K chunks and 4 column
     // blocks of 128, so all of B fits next to a ring of at least 2 A tiles,
     // and there are enough row tiles to keep every SM busy.

@@ -42,7 +42,7 @@ def test_stage_counts_bit_identical_bn256():
     M, N, K = 2560, 2048, 520          # enough tiles for the 256-wide tile; ragged K
     a, b = seeded_case(M, N, K, "bf16", seed=21, dist=("uniform", -1.0, 1.0))
     p = _plan(M, N, K, "bf16", "bf16")
-    assert p["block_n"] == 256 and p["max_stages"] >= 4
+    assert p["block_n"] == 256 and p["max_stages"] >= 4  # the planner's own choice here
     outs = [run_gpu(a, b, M, N, K, "bf16", "bf16", stages=s) for s in (1, 2, 3, 4)]
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
@@ -111,6 +111,20 @@ def test_stage_counts_bit_identical_bn192():
         assert np.array_equal(o, outs[0])
     ref, _, S = oracle.gemm(a, b, "bf16", "f32", K=K)
     compare(outs[0], ref, S, "f32", "bn192")
+
+
+def test_planner_tile_widths():
+    """The planner's width choice counts whole waves of tiles: 2048^3 fills
+    fewer SMs with 256-wide tiles than with 128-wide ones, but 128-wide tiles
+    stage twice the operand bytes per product, so 256 (paired) wins; a
+    1000^3 problem fits in one wave either way and keeps 128; a short K loop
+    keeps 128 for the epilogue's sake."""
+    p = _plan(2048, 2048, 2048, "f16", "f16")
+    assert p["block_n"] == 256 and p["pair_mma"] == 1
+    p = _plan(8192, 8192, 8192, "bf16", "bf16")
+    assert p["block_n"] == 256 and p["pair_mma"] == 1
+    assert _plan(1000, 1000, 1000, "f16", "f16")["block_n"] == 128
+    assert _plan(8192, 8192, 256, "f16", "f16")["block_n"] == 128
 
 
 def test_paired_mma_small():
