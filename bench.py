@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg (profiling runs)")
     ap.add_argument("--no-secondary", action="store_true", help="skip the other-workload summary")
+    ap.add_argument("--no-library-reference", action="store_true",
+                    help="skip the same-run torch.matmul (cuBLAS) reference of tensor-bound workloads")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--tune", action="store_true",
                     help="tune the launch configuration first (sg_tune) instead of the planner's heuristic")
@@ -379,6 +381,40 @@ def dram_reference(device, nbytes_write: int, steps: int = 10):
             "bytes": 2 * n, "how": "cudaMemsetAsync of the output's bytes; device copy of as many bytes (read+write)"}
 
 
+def library_reference(w, dev_tensors, stream, steps=10, warmup=3):
+    """Same-run library reference for a tensor-bound fp16/bf16 workload: the
+    same product through torch.matmul (cuBLAS) plus torch's own ReLU / bias
+    ops for the epilogue, on the same device tensors, timed like the GEMM (L2
+    flushed before each step, CUDA events).  Context only: it is not the
+    product path and not the driver's reference arm."""
+    import torch
+    if w.name in HBM_BOUND or w.in_dtype == "e4m3" or w.dist_r is not None:
+        return None
+    A, B, bias, C = dev_tensors
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=A.device)
+
+    def call():
+        if w.epilogue == "bias_relu":
+            torch.addmm(bias.to(C.dtype), A, B, out=C)
+        else:
+            torch.matmul(A, B, out=C)
+        if w.epilogue != "none":
+            C.relu_()
+
+    def flush():
+        flush_buf.fill_(1)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush()
+            call()
+        torch.cuda.synchronize()
+        times = time_steps(call, steps, stream, flush)
+    ms = sum(times) / len(times)
+    return {"impl": "torch.matmul (cuBLAS)" + (" + torch ReLU" if w.epilogue != "none" else ""),
+            "value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms}
+
+
 def roofline_of(w, ms, peaks, traffic):
     if w.name in HBM_BOUND:
         achieved = w.algorithmic_bytes / (ms * 1e-3) / 1e9
@@ -443,6 +479,12 @@ def main():
     plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages)
     plan["tuned"] = args.tune and args.stages == 0 and w.dist_r is None
 
+    lib_ref = None
+    if rank == 0 and not args.no_library_reference:
+        lib_ref = library_reference(w, dev_tensors, stream)
+        if lib_ref is not None:
+            lib_ref["ours_over_library"] = (w.flops / (ms * 1e-3) / 1e12) / lib_ref["value"]
+
     e2e = None
     if not args.no_e2e:
         del dev_tensors
@@ -464,6 +506,8 @@ def main():
         "e2e": e2e,
         "kernel_source_hash": kernel_source_hash(),
     }
+    if lib_ref is not None:
+        line["library_reference"] = lib_ref
     if w.name in HBM_BOUND:
         line["hbm_gbs"] = line["roofline"]["achieved"]
         out_bytes = w.M * w.N * {"f32": 4, "f16": 2, "bf16": 2}[w.out_dtype]
@@ -474,10 +518,15 @@ def main():
         for name in ("relu4096_f16", "swin4k_proj_f16", "swin4k_backproj_f16", "square8192_e4m3"):
             ws = gemm_inputs.WORKLOADS[name]
             t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=args.tune)
-            del dt
             m2 = sum(t2) / len(t2)
-            sec.append({"workload": name, "ms_per_step": m2, "TFLOP/s": ws.flops / (m2 * 1e-3) / 1e12,
-                        "roofline": roofline_of(ws, m2, peaks, recorded_traffic(name))})
+            entry = {"workload": name, "ms_per_step": m2, "TFLOP/s": ws.flops / (m2 * 1e-3) / 1e12,
+                     "roofline": roofline_of(ws, m2, peaks, recorded_traffic(name))}
+            lr = None if args.no_library_reference else library_reference(ws, dt, stream)
+            if lr is not None:
+                lr["ours_over_library"] = entry["TFLOP/s"] / lr["value"]
+                entry["library_reference"] = lr
+            del dt
+            sec.append(entry)
         line["secondary"] = sec
 
     if rank == 0 and not args.no_cpu_baseline and world >= 1:
