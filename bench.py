@@ -491,7 +491,7 @@ def main():
         e2e_ms, h2d, d2h = measure_e2e(sg, w, host_inputs, device, stream, max(3, min(args.steps, 10)), args.stages)
         e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "api": "tensor_core_gemm_tma_gb300.stage_gemm_host (pinned host buffers)"}
+               "api": "tensor_core_gemm_tma_gb300.stage_gemm_host -> sg_gemm_host (C ABI; pinned host buffers, row-chunked copies overlapped with the GEMMs)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

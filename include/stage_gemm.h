@@ -38,7 +38,10 @@
  *
  * Ownership: the caller owns A, B, C and bias (device memory, e.g. from
  * PyTorch).  The library never frees caller memory.  It allocates, once per
- * device, a 4-byte device status word and keeps host-side caches.
+ * device, a 4-byte device status word and keeps host-side caches;
+ * sg_gemm_host also creates, once per device, three streams and five events,
+ * and allocates one stream-ordered device buffer per call (released on the
+ * call's stream).
  *
  * Execution: every call is asynchronous on `stream` (a cudaStream_t passed as
  * void*; NULL is the legacy default stream).  Argument checks run on the
@@ -148,6 +151,41 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K,
                      void* C, int64_t ldc,
                      int in_dtype, int out_dtype, int epilogue,
                      const float* bias, int stages, void* stream);
+
+/*
+ * sg_gemm_host -- the same product, C = epilogue(A . B [+ R]), on HOST
+ * buffers: A, B, R (may be NULL: no residual), bias and C are host pointers
+ * with the meanings, layouts and pitches of sg_gemm / sg_gemm_residual.
+ * The pages define only the product; this call adds the transfers around
+ * it.  It allocates one device buffer (stream-ordered, cudaMallocAsync on
+ * `stream`, released with cudaFreeAsync on the same stream), copies bias
+ * and B in, then copies A (and R) in row chunks on a library-owned stream
+ * while each chunk's GEMM runs as soon as its rows have arrived (chunks
+ * alternate between `stream` and a library-owned compute stream, so one
+ * chunk's last wave overlaps the next chunk's first), and copies each chunk
+ * of C back on another library-owned stream while later chunks compute.  A
+ * host pitch that is a whole number of 16-byte units is kept on the device
+ * and each chunk then moves as one contiguous span; other pitches move row
+ * by row.  All of it is ordered after the work already on `stream`, and
+ * `stream` waits for all of it: synchronise `stream` before reading C or
+ * releasing the host buffers.  Page-locked host memory
+ * lets the copies overlap the GEMMs; pageable memory works, with the copies
+ * staged by the driver.  The chunks are GEMMs over row ranges of the same
+ * operands, so every element of C has the same bits as from sg_gemm.
+ * Concurrent calls on one device are serialised while they are queued (the
+ * library's copy streams and events are shared).  The environment variable
+ * STAGE_GEMM_HOST_CHUNKS (1..64) overrides the chunk count (tuning only).
+ * Returns the codes of sg_gemm and sg_gemm_residual (host-side checks,
+ * including the overlap rules, apply to the host ranges); SG_ERR_CUDA when
+ * an allocation, copy or launch fails.
+ */
+int sg_gemm_host(int64_t M, int64_t N, int64_t K,
+                 const void* A, int64_t lda,
+                 const void* B, int64_t ldb,
+                 const void* R, int64_t ldr,
+                 void* C, int64_t ldc,
+                 int in_dtype, int out_dtype, int epilogue,
+                 const float* bias, int stages, void* stream);
 
 /* The launch configuration sg_gemm would use for TMA-legal A and B (no GPU
  * work is queued).  Needs a current CUDA device; returns the same codes as

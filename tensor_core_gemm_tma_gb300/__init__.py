@@ -70,6 +70,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.sg_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
         lib.sg_gemm_residual.restype = i32
         lib.sg_gemm_residual.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
+        lib.sg_gemm_host.restype = i32
+        lib.sg_gemm_host.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
         lib.sg_plan.restype = i32
         lib.sg_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i64, vp, ctypes.POINTER(PlanInfo)]
         lib.sg_device_status.restype = i32
@@ -196,21 +198,52 @@ def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: 
 
 def stage_gemm_host(A_host, B_host, out_dtype=None, epilogue: str = "none", bias_host=None, stages: int = 0,
                     device=None, stream=None, out_host=None, residual_host=None):
-    """End-to-end call on host tensors: copies A, B (bias, residual) to the
-    device, runs ``stage_gemm`` and copies C back into ``out_host`` (pinned
-    host memory is used for asynchronous copies).  Returns the host tensor."""
+    """C = epilogue(A @ B [+ residual]) on HOST tensors through the C ABI's
+    host-buffer call (sg_gemm_host): the library copies bias and B in, then
+    A (and the residual) in row chunks whose GEMMs run on ``stream`` as the
+    rows arrive, and copies each chunk of C back into ``out_host`` while
+    later chunks compute.  Asynchronous: synchronise ``stream`` before
+    reading ``out_host``, and keep the host tensors alive until then.
+    Page-locked (pinned) host tensors let the copies overlap the GEMMs.
+    ``out_host`` defaults to a new pinned M x N tensor of ``out_dtype``
+    (float32 if not given).  Returns ``out_host``."""
     torch = _torch()
     dev = torch.device(device or "cuda")
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    with torch.cuda.stream(s):
-        A = A_host.to(dev, non_blocking=True)
-        B = B_host.to(dev, non_blocking=True)
-        bias = None if bias_host is None else bias_host.to(dev, non_blocking=True)
-        R = None if residual_host is None else residual_host.to(dev, non_blocking=True)
-        C = stage_gemm(A, B, out_dtype=out_dtype, epilogue=epilogue, bias=bias, stages=stages, stream=s, residual=R)
-        if out_host is None:
-            out_host = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
-        out_host.copy_(C, non_blocking=True)
+    for t in (A_host, B_host):
+        if t.device.type != "cpu":
+            raise ValueError("A_host and B_host must be CPU tensors")
+    if A_host.dtype != B_host.dtype:
+        raise ValueError("A and B must have the same dtype")
+    M, K = A_host.shape
+    K2, N = B_host.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out_host is None:
+        out_host = torch.empty((M, N), dtype=out_dtype or torch.float32, pin_memory=True)
+    elif out_dtype is not None and out_host.dtype != out_dtype:
+        raise ValueError("out_host has a different dtype from out_dtype")
+    if out_host.device.type != "cpu" or tuple(out_host.shape) != (M, N):
+        raise ValueError("out_host must be an M x N CPU tensor")
+    if epilogue not in EPILOGUES:
+        raise ValueError(f"epilogue must be one of {sorted(EPILOGUES)}")
+    bptr = None
+    if bias_host is not None:
+        if (bias_host.dtype != torch.float32 or bias_host.device.type != "cpu" or bias_host.numel() != N
+                or not bias_host.is_contiguous()):
+            raise ValueError("bias_host must be a contiguous fp32 CPU vector of N values")
+        bptr = bias_host.data_ptr()
+    rptr, ldr = None, 0
+    if residual_host is not None:
+        if (residual_host.dtype != out_host.dtype or tuple(residual_host.shape) != (M, N)
+                or residual_host.device.type != "cpu"):
+            raise ValueError("residual_host must be an M x N CPU tensor of the output dtype")
+        rptr, ldr = residual_host.data_ptr(), _row_pitch(residual_host)
+    with torch.cuda.device(dev):
+        rc = load_library().sg_gemm_host(
+            M, N, K, A_host.data_ptr(), _row_pitch(A_host), B_host.data_ptr(), _row_pitch(B_host), rptr, ldr,
+            out_host.data_ptr(), _row_pitch(out_host), dtype_code(A_host.dtype), dtype_code(out_host.dtype),
+            EPILOGUES[epilogue], bptr, int(stages), _stream_ptr(stream, dev).value)
+    _check(rc)
     return out_host
 
 

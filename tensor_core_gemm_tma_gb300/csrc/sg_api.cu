@@ -1,6 +1,7 @@
 // sg_api.cu -- host side of the C ABI declared in include/stage_gemm.h:
 // argument checks, the launch plan (tile width, stage count, persistent grid),
-// the TMA tensor-map builder and the kernel launch.
+// the TMA tensor-map builder, the kernel launch, and the host-buffer entry
+// (chunked copies overlapped with the GEMMs).
 //
 // Every argument check runs before the first CUDA call, so a rejected call
 // never touches the device.
@@ -43,9 +44,14 @@ struct DevState {
     // per kernel instantiation [tile width][output type][mode - 1][residual]:
     bool attr_done[2][3][3][4][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
     int max_clusters[2][3][3][4][2] = {};  // the same index: co-resident clusters (0: not queried)
+    // sg_gemm_host: library-owned copy streams, a second compute stream and
+    // events, created on first use
+    cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_in = nullptr, ev_gemm = nullptr, ev_out = nullptr, ev_comp = nullptr;
 };
 
 std::mutex g_mu;
+std::mutex g_host_mu;  // serialises sg_gemm_host calls while they queue work
 DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -151,6 +157,48 @@ int device_state(DevState** out) {
     }
     *out = &st;
     return SG_OK;
+}
+
+// The copy streams and events of sg_gemm_host, once per device.
+int host_streams(DevState& st) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (st.h2d) return SG_OK;
+    cudaStream_t q[3] = {};
+    cudaEvent_t e[5] = {};
+    bool ok = true;
+    for (auto& x : q) ok = ok && cudaStreamCreateWithFlags(&x, cudaStreamNonBlocking) == cudaSuccess;
+    for (auto& ev : e) ok = ok && cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        for (auto& x : q)
+            if (x) cudaStreamDestroy(x);
+        for (auto& ev : e)
+            if (ev) cudaEventDestroy(ev);
+        return SG_ERR_CUDA;
+    }
+    st.ev_fork = e[0];
+    st.ev_in = e[1];
+    st.ev_gemm = e[2];
+    st.ev_out = e[3];
+    st.ev_comp = e[4];
+    st.d2h = q[1];
+    st.comp = q[2];
+    st.h2d = q[0];  // last: a non-null h2d marks the set as complete
+    return SG_OK;
+}
+
+// Row chunks of sg_gemm_host: about one per 32 MB of copies, at most 16,
+// each a whole number of 256-row pair tiles; STAGE_GEMM_HOST_CHUNKS (1..64)
+// overrides the count.  On GB300 (host link ~210 GB/s each way) 8-24 chunks
+// were within 2% of each other for 8192^3 and for M=518400, K=96, N=384.
+int64_t host_chunk_rows(int64_t M, uint64_t copy_bytes) {
+    int64_t n = static_cast<int64_t>(copy_bytes / (32ull << 20));
+    n = std::max<int64_t>(1, std::min<int64_t>(16, n));
+    if (const char* e = std::getenv("STAGE_GEMM_HOST_CHUNKS")) {
+        const int x = std::atoi(e);
+        if (x >= 1 && x <= 64) n = x;
+    }
+    const int64_t rows = cdiv(cdiv(M, n), 2 * sg::BM) * (2 * sg::BM);
+    return std::max<int64_t>(rows, 1);
 }
 
 // A launch configuration chosen by sg_tune (or forced): every field
@@ -516,6 +564,115 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
     if ((rc = device_state(&st)) != SG_OK) return rc;
     return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
                            g_skip_load.load(), static_cast<cudaStream_t>(stream), nullptr, nullptr, R, ldr);
+}
+
+int sg_gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                 const void* R, int64_t ldr, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue,
+                 const float* bias, int stages, void* stream) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    const int esz = elem_bytes(in_dtype), oes = elem_bytes(out_dtype);
+    if (R) {
+        if (ldr < N || ldr > 0x7FFFFFFF) return SG_ERR_ARG;
+        if (reinterpret_cast<uintptr_t>(R) % oes) return SG_ERR_ALIGN;
+        const bool same = (R == C && ldr == ldc);
+        if (!same && overlap(C, span_bytes(M, N, ldc, oes), R, span_bytes(M, N, ldr, oes))) return SG_ERR_ALIAS;
+    }
+    DevState* st = nullptr;
+    if ((rc = device_state(&st)) != SG_OK) return rc;
+    if ((rc = host_streams(*st)) != SG_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // Device copies keep the host pitch when it is a whole number of 16-byte
+    // units (each chunk then moves as one contiguous span of the host
+    // operand; the padding columns it carries are never read); otherwise the
+    // rows are packed to a 16-byte pitch by a 2-D copy.  Every operand and
+    // every row chunk of it is then TMA-legal.  C returns as one span only
+    // when it has no padding columns, so the caller's padding is never
+    // written.
+    auto dev_pitch = [](int64_t ld, int64_t cols, int e) {
+        return (ld * e) % 16 == 0 ? ld : cdiv(std::max<int64_t>(cols, 1), 16 / e) * (16 / e);
+    };
+    auto up = [](uint64_t b) { return (b + 255) & ~uint64_t(255); };
+    const int64_t pa = dev_pitch(lda, K, esz), pb = dev_pitch(ldb, N, esz), pc = dev_pitch(ldc, N, oes);
+    const int64_t pr = R ? dev_pitch(ldr, N, oes) : 0;
+    const uint64_t a_bytes = K > 0 ? up(uint64_t(M) * pa * esz) : 0;
+    const uint64_t b_bytes = K > 0 ? up(uint64_t(K) * pb * esz) : 0;
+    const uint64_t c_bytes = up(uint64_t(M) * pc * oes);
+    const uint64_t r_bytes = R ? up(uint64_t(M) * pr * oes) : 0;
+    const uint64_t bias_bytes = bias ? up(uint64_t(N) * 4) : 0;
+    const uint64_t total = a_bytes + b_bytes + c_bytes + r_bytes + bias_bytes;
+    const uint64_t copy_bytes = uint64_t(M) * K * esz + uint64_t(K) * N * esz + uint64_t(M) * N * oes * (R ? 2 : 1);
+    const int64_t chunk = host_chunk_rows(M, copy_bytes);
+
+    std::lock_guard<std::mutex> lk(g_host_mu);
+    char* buf = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&buf), total, s) != cudaSuccess) return SG_ERR_CUDA;
+    char* dA = K > 0 ? buf : nullptr;
+    char* dB = K > 0 ? buf + a_bytes : nullptr;
+    char* dC = buf + a_bytes + b_bytes;
+    char* dR = R ? dC + c_bytes : nullptr;
+    float* dbias = bias ? reinterpret_cast<float*>(dC + c_bytes + r_bytes) : nullptr;
+    const char* hA = static_cast<const char*>(A);
+    const char* hR = static_cast<const char*>(R);
+    char* hC = static_cast<char*>(C);
+    // rows [r0, r0 + rows) of a cols-wide operand between pitches hp and dp
+    auto copy_rows = [&](void* dst, int64_t dp, const void* src, int64_t hp, int64_t cols, int e, int64_t rows,
+                         cudaMemcpyKind kind, cudaStream_t on, bool span_ok) {
+        const int64_t sp = kind == cudaMemcpyHostToDevice ? hp : dp, tp = kind == cudaMemcpyHostToDevice ? dp : hp;
+        if (span_ok && sp == tp)
+            return cudaMemcpyAsync(dst, src, span_bytes(rows, cols, sp, e), kind, on) == cudaSuccess;
+        return cudaMemcpy2DAsync(dst, tp * e, src, sp * e, cols * e, rows, kind, on) == cudaSuccess;
+    };
+    const auto H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+
+    // fork: the copy streams start after the work already on `stream`
+    bool ok = cudaEventRecord(st->ev_fork, s) == cudaSuccess &&
+              cudaStreamWaitEvent(st->h2d, st->ev_fork, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(st->d2h, st->ev_fork, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(st->comp, st->ev_fork, 0) == cudaSuccess;
+    if (ok && bias) ok = cudaMemcpyAsync(dbias, bias, size_t(N) * 4, H2D, st->h2d) == cudaSuccess;
+    if (ok && K > 0) ok = copy_rows(dB, pb, B, ldb, N, esz, K, H2D, st->h2d, true);
+    // Chunks alternate between `stream` and the library's second compute
+    // stream, so a chunk's CTAs take SMs as the previous chunk's last wave
+    // leaves them (one CTA per SM either way: each holds more than half the
+    // shared memory and all of the tensor memory).
+    int gemm_rc = SG_OK;
+    int64_t idx = 0;
+    for (int64_t r0 = 0; ok && r0 < M; r0 += chunk, ++idx) {
+        const int64_t rows = std::min(chunk, M - r0);
+        cudaStream_t cs = (idx % 2 == 0) ? s : st->comp;
+        if (K > 0) ok = copy_rows(dA + r0 * pa * esz, pa, hA + r0 * lda * esz, lda, K, esz, rows, H2D, st->h2d, true);
+        if (ok && R)
+            ok = copy_rows(dR + r0 * pr * oes, pr, hR + r0 * ldr * oes, ldr, N, oes, rows, H2D, st->h2d, true);
+        ok = ok && cudaEventRecord(st->ev_in, st->h2d) == cudaSuccess &&
+             cudaStreamWaitEvent(cs, st->ev_in, 0) == cudaSuccess;
+        if (!ok) break;
+        gemm_rc = plan_and_launch(*st, rows, N, K, K > 0 ? dA + r0 * pa * esz : nullptr, pa, dB, pb,
+                                  dC + r0 * pc * oes, pc, in_dtype, out_dtype, epilogue, dbias, stages,
+                                  g_skip_load.load(), cs, nullptr, nullptr, R ? dR + r0 * pr * oes : nullptr, pr);
+        if (gemm_rc != SG_OK) break;
+        ok = cudaEventRecord(st->ev_gemm, cs) == cudaSuccess &&
+             cudaStreamWaitEvent(st->d2h, st->ev_gemm, 0) == cudaSuccess &&
+             copy_rows(hC + r0 * ldc * oes, pc, dC + r0 * pc * oes, ldc, N, oes, rows, D2H, st->d2h, ldc == N);
+    }
+    // join (also after a failure, so nothing queued outlives the buffer):
+    // `stream` waits for both copy streams, then releases the buffer
+    bool joined = cudaEventRecord(st->ev_out, st->d2h) == cudaSuccess &&
+                  cudaStreamWaitEvent(s, st->ev_out, 0) == cudaSuccess &&
+                  cudaEventRecord(st->ev_in, st->h2d) == cudaSuccess &&
+                  cudaStreamWaitEvent(s, st->ev_in, 0) == cudaSuccess &&
+                  cudaEventRecord(st->ev_comp, st->comp) == cudaSuccess &&
+                  cudaStreamWaitEvent(s, st->ev_comp, 0) == cudaSuccess;
+    if (!joined) {
+        cudaStreamSynchronize(st->d2h);
+        cudaStreamSynchronize(st->h2d);
+        cudaStreamSynchronize(st->comp);
+    }
+    const bool freed = cudaFreeAsync(buf, s) == cudaSuccess;
+    if (gemm_rc != SG_OK) return gemm_rc;
+    return (ok && joined && freed) ? SG_OK : SG_ERR_CUDA;
 }
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages, int64_t ldc,

@@ -135,3 +135,23 @@ def test_rejects_element_misalignment(sg):
     # staged by element loads and needs a GPU, so it is tested there)
     assert call(sg, A=P16 + 1) == -5
     assert call(sg, B=P16B + 3) == -5
+
+
+@needs_no_gpu
+def test_host_entry_rejects_bad_args(sg):
+    """sg_gemm_host applies sg_gemm's checks and the residual's to the host
+    ranges before any CUDA call."""
+    f = sg.load_library().sg_gemm_host
+
+    def call(M=64, N=64, K=64, A=P16, lda=64, B=P16B, ldb=64, R=None, ldr=0, C=PC, ldc=64, ind=1, outd=1, epi=0,
+             bias=None):
+        return f(M, N, K, A, lda, B, ldb, R, ldr, C, ldc, ind, outd, epi, bias, 0, None)
+
+    assert call(M=0, A=None, B=None, C=None) == 0          # empty: a no-op
+    assert call(lda=63) == -1
+    assert call(ind=0) == -2                                # fp32 operands
+    assert call(epi=2) == -1                                # bias missing
+    assert call(C=P16 + 64) == -4                           # C overlaps A
+    assert call(R=0x5000000, ldr=10) == -1                  # ldr < N
+    assert call(R=PC + 1, ldr=64) == -5                     # residual not aligned to its 2-byte elements
+    assert call(R=PC + 2, ldr=64) == -4                     # residual partly overlapping C
