@@ -180,6 +180,7 @@ def test_torch_api_matches_raw_path():
     ref, _, S = oracle.gemm(a, b, "bf16", "bf16", "relu")
     compare(got, ref, S, "bf16", "torch-api")
     # end-to-end host path
-    Ch = sg.stage_gemm_host(A.cpu().pin_memory(), B.cpu().pin_memory(), out_dtype=torch.bfloat16, epilogue="relu")
+    Ah, Bh = A.cpu().pin_memory(), B.cpu().pin_memory()  # alive until the stream has finished with them
+    Ch = sg.stage_gemm_host(Ah, Bh, out_dtype=torch.bfloat16, epilogue="relu")
     torch.cuda.synchronize()
     assert torch.equal(Ch.view(torch.int16), C.cpu().view(torch.int16))
