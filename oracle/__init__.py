@@ -76,6 +76,8 @@ def _load():
         lib.orc_gemm_at.restype = i32
         lib.orc_gemm_at.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, i32, vp, i32, i64, vp, vp, vp, dp, dp,
                                     i32]
+        lib.orc_gemm_qb.restype = i32
+        lib.orc_gemm_qb.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64, vp, i32, vp, i32, vp, i64, dp, dp, i32]
         lib.orc_decode_array.restype = None
         lib.orc_decode_array.argtypes = [i32, vp, i64, dp]
         lib.orc_encode_array.restype = None
@@ -171,6 +173,40 @@ def gemm(A_bits: np.ndarray, B_bits: np.ndarray, in_dtype: str, out_dtype: str, 
                                    _threads(threads))
     if rc != 0:
         raise ValueError(f"orc_gemm rejected its arguments (rc={rc})")
+    return C, exact, S
+
+
+def gemm_qb(A_bits: np.ndarray, Q: np.ndarray, scale: np.ndarray, in_dtype: str, out_dtype: str,
+            epilogue: str = "none", bias: np.ndarray | None = None, K: int | None = None, N: int | None = None,
+            threads: int | None = None):
+    """Product with an integer-coded B (Tolk.Stage, "Decoded panels on the
+    host"): Q holds int8 codes (K x ldq), ``scale`` one fp32 value per
+    column, and b_kj = scale_j * q_kj.  A_bits is M x lda of ``in_dtype``.
+    Returns (C_bits, C_exact, S) as ``gemm`` does (C dense M x N)."""
+    if A_bits.ndim != 2 or Q.ndim != 2:
+        raise ValueError("A and Q must be 2-D")
+    if A_bits.dtype != _NP_BITS[in_dtype] or Q.dtype != np.int8:
+        raise ValueError(f"A holds {in_dtype} patterns and Q int8 codes")
+    for X in (A_bits, Q):
+        if X.size > 0 and X.shape[1] > 1 and X.strides[1] != X.itemsize:
+            raise ValueError("rows of A and Q must be contiguous")
+    M = A_bits.shape[0]
+    K = A_bits.shape[1] if K is None else int(K)
+    N = Q.shape[1] if N is None else int(N)
+    if Q.shape[0] < K:
+        raise ValueError("Q has fewer than K rows")
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    if s.size < N:
+        raise ValueError("scale has fewer than N values")
+    C = np.zeros((M, N), dtype=_NP_BITS[out_dtype])
+    exact = np.empty((M, N), dtype=np.float64)
+    S = np.empty((M, N), dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    rc = _load().orc_gemm_qb(M, N, K, _ptr(A_bits), _ld(A_bits), _DT[in_dtype], _ptr(Q), _ld(Q), _ptr(s),
+                             _EPI[epilogue], _ptr(b), _DT[out_dtype], _ptr(C), N, _ptr(exact), _ptr(S),
+                             _threads(threads))
+    if rc != 0:
+        raise ValueError(f"orc_gemm_qb rejected its arguments (rc={rc})")
     return C, exact, S
 
 

@@ -40,6 +40,9 @@
  *     s_ij = R_ij + sum_k a_ik b_kj, before the bias and the ReLU: the
  *     fold starts from R instead of zeros (gizml:tile, "Program.fold",
  *     init), so K = 0 gives C = epilogue(R [+ bias]).
+ *   - Integer-coded B (orc_gemm_qb): Tolk.Stage, "Decoded panels on the
+ *     host" -- an operand decoded from integer codes, as a quantised
+ *     matrix's is; read here as int8 codes times one fp32 scale per column.
  *   - Staging never changes values (Tolk.Stage, module overview): the oracle
  *     has no staging at all; the GPU path's results at every stage count are
  *     graded against this one definition.
@@ -249,6 +252,10 @@ static double *decode_matrix(int dtype, const void *X, int64_t rows, int64_t col
     return out;
 }
 
+static int run_decoded(int64_t M, int64_t N, int64_t K, const double *Ad, const double *Bd, const void *R,
+                       int r_dtype, int64_t ldr, int epi, const float *bias, int out_dtype, void *C, int64_t ldc,
+                       double *C_exact, double *S, int threads);
+
 /* C[i*ldc + j] = encode(out_dtype, epilogue(R_ij + sum_k a_ik b_kj)) for
  * i < M, j < N, with R_ij = 0 when R is NULL.  C_exact and S, when given,
  * receive the fp64 value before rounding and the sum of |a_ik b_kj| (dense
@@ -269,6 +276,17 @@ int orc_gemm_residual(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         free(Bd);
         return -2;
     }
+    const int rc = run_decoded(M, N, K, Ad, Bd, R, r_dtype, ldr, epi, bias, out_dtype, C, ldc, C_exact, S, threads);
+    free(Ad);
+    free(Bd);
+    return rc;
+}
+
+/* The row loop of the GEMM on decoded (fp64, dense) operands, split over
+ * POSIX threads by whole rows. */
+static int run_decoded(int64_t M, int64_t N, int64_t K, const double *Ad, const double *Bd, const void *R,
+                       int r_dtype, int64_t ldr, int epi, const float *bias, int out_dtype, void *C, int64_t ldc,
+                       double *C_exact, double *S, int threads) {
     if (threads < 1) threads = 1;
     if (threads > M) threads = (int)M;
     gemm_job *jobs = (gemm_job *)calloc((size_t)threads, sizeof(gemm_job));
@@ -303,6 +321,42 @@ int orc_gemm_residual(int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     }
     free(jobs);
     free(tids);
+    return rc;
+}
+
+/* ------------------------------------------------ integer-coded B operand
+ *
+ * Tolk.Stage, "Decoded panels on the host": one operand of the product is
+ * decoded from integer codes, as a quantised matrix's is.  The page names no
+ * code format; the reading taken here: B is given as signed 8-bit codes q_kj
+ * (two's complement, row-major K x N, pitch ldq) and one fp32 scale s_j per
+ * column, and its value is b_kj = s_j * q_kj.  That product is exact in fp64
+ * (24 + 8 significant bits), so the decoded B below is the value itself and
+ * the rest is orc_gemm's definition: C = epilogue(sum_k a_ik b_kj), S_ij =
+ * sum_k |a_ik b_kj|.  Where the decode happens (once per panel, as the page
+ * stages it, or at every use) cannot change the value; the oracle has no
+ * panel at all. */
+int orc_gemm_qb(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int in_dtype, const int8_t *Q,
+                int64_t ldq, const float *scale, int epi, const float *bias, int out_dtype, void *C, int64_t ldc,
+                double *C_exact, double *S, int threads) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (!valid_in(in_dtype) || !valid_out(out_dtype) || !valid_epi(epi)) return -1;
+    if ((epi == ORC_EPI_BIAS_RELU) != (bias != NULL)) return -1;
+    if (lda < K || ldq < N || ldc < N || (N > 0 && !scale)) return -1;
+    if (M == 0 || N == 0) return 0;
+    double *Ad = decode_matrix(in_dtype, A, M, K, lda);
+    double *Bd = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
+    if (!Ad || !Bd) {
+        free(Ad);
+        free(Bd);
+        return -2;
+    }
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < N; ++j) {
+            const double s_j = orc_decode(ORC_FP32, load_bits(ORC_FP32, scale, j));
+            Bd[k * N + j] = s_j * (double)Q[k * ldq + j];
+        }
+    const int rc = run_decoded(M, N, K, Ad, Bd, NULL, ORC_FP32, 0, epi, bias, out_dtype, C, ldc, C_exact, S, threads);
     free(Ad);
     free(Bd);
     return rc;
