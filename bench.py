@@ -43,7 +43,7 @@ import gemm_inputs  # noqa: E402
 L2_FLUSH_BYTES = 256 << 20
 METRIC = "GEMM TFLOP/s and % of GB300 dense fp16/bf16 peak (HBM GB/s for skinny-K)"
 DEFAULT_WORKLOAD = "square8192_bf16"
-HBM_BOUND = {"swin4k_proj_f16", "swin4k_backproj_f16"}
+HBM_BOUND = {"swin4k_proj_f16", "swin4k_backproj_f16", "swin4k_proj_i8w"}
 
 
 def parse():
@@ -167,14 +167,18 @@ class ClockSampler:
 def device_inputs(w, device):
     """Host tensors of the workload's operands: (A, B, bias, R)."""
     import torch
-    a, b, bias, r = w.a_bits(), w.b_bits(), w.bias(), w.r_bits()
+    a, bias, r = w.a_bits(), w.bias(), w.r_bits()
     if w.in_dtype == "e4m3":
         A = torch.from_numpy(a).view(torch.float8_e4m3fn)
-        B = torch.from_numpy(b).view(torch.float8_e4m3fn)
+        B = torch.from_numpy(w.b_bits()).view(torch.float8_e4m3fn)
     else:
         tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[w.in_dtype]
         A = torch.from_numpy(a.view(np.int16)).view(tdt)
-        B = torch.from_numpy(b.view(np.int16)).view(tdt)
+        if w.b_coded:  # (int8 codes, per-column fp32 scales)
+            q, sc = w.b_codes()
+            B = (torch.from_numpy(q), torch.from_numpy(sc))
+        else:
+            B = torch.from_numpy(w.b_bits().view(np.int16)).view(tdt)
     bias_t = None if bias is None else torch.from_numpy(bias.copy())
     R = None
     if r is not None:
@@ -200,20 +204,33 @@ def time_steps(call, steps, stream, flush):
     return [s.elapsed_time(e) for s, e in evs]
 
 
+def b_operand(w):
+    """B as the oracle takes it: bit patterns, or (int8 codes, scales)."""
+    return w.b_codes() if w.b_coded else w.b_bits()
+
+
+def oracle_rows(w, a, b, bias, r, rows, threads):
+    """The oracle (as it stands) on rows 0..rows-1 of the workload."""
+    import oracle
+    if w.b_coded:
+        q, s = b
+        return oracle.gemm_qb(a[:rows], q, s, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads)
+    return oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads,
+                       R_bits=None if r is None else r[:rows], r_dtype=w.out_dtype if r is not None else None)
+
+
 def cpu_oracle_sample(w, target_s=12.0, a=None, b=None, bias=None):
     """Time the oracle (as it stands) on a row-block sample of the workload:
     returns (seconds, rows, flops, threads)."""
-    import oracle
     a = w.a_bits() if a is None else a
-    b = w.b_bits() if b is None else b
+    b = b_operand(w) if b is None else b
     bias = w.bias() if bias is None else bias
     r = w.r_bits()
     threads = os.cpu_count() or 1
     rows = min(w.M, max(threads, 16))
     while True:
         t0 = time.perf_counter()
-        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads,
-                    R_bits=None if r is None else r[:rows], r_dtype=w.out_dtype if r is not None else None)
+        oracle_rows(w, a, b, bias, r, rows, threads)
         dt = time.perf_counter() - t0
         if dt >= target_s / 4 or rows >= w.M:
             break
@@ -225,15 +242,13 @@ def run_reference(args, w, rank, world):
     """The oracle arm: rank 0 only, on the host cores."""
     if rank != 0:
         return
-    a, b, bias, r = w.a_bits(), w.b_bits(), w.bias(), w.r_bits()
+    a, b, bias, r = w.a_bits(), b_operand(w), w.bias(), w.r_bits()
     # size one step's sample from a calibration run
     _, rows, _, threads = cpu_oracle_sample(w, target_s=4.0, a=a, b=b, bias=bias)
-    import oracle
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.gemm(a[:rows], b, w.in_dtype, w.out_dtype, w.epilogue, bias, threads=threads,
-                    R_bits=None if r is None else r[:rows], r_dtype=w.out_dtype if r is not None else None)
+        oracle_rows(w, a, b, bias, r, rows, threads)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -263,7 +278,9 @@ def config_of(w, plan):
         c["stages"] = plan["stages"]
         c["grid"] = plan["grid"]
         c["kernel_mode"] = {1: "single CTA", 2: "CTA pair, B multicast", 3: "paired MMA (cta_group::2)",
-                            4: "resident B (one CTA per row tile, all of B in shared memory)"}.get(plan.get("mode"))
+                            4: "resident B (one CTA per row tile, all of B in shared memory)",
+                            5: "decoded panel (int8-coded B decoded once per CTA into the resident shared-memory "
+                               "panel)"}.get(plan.get("mode"))
         c["raster_group_m"] = plan.get("group_m")
         c["tuned"] = plan.get("tuned", False)
     return c
@@ -273,17 +290,20 @@ def measure(sg, w, device, stream, steps, warmup, stages, inputs=None, tune=True
     import torch
     A_h, B_h, bias_h, R_h = inputs if inputs is not None else device_inputs(w, device)
     A = A_h.to(device)
-    B = B_h.to(device)
+    B = tuple(x.to(device) for x in B_h) if w.b_coded else B_h.to(device)
     bias = None if bias_h is None else bias_h.to(device)
     R = None if R_h is None else R_h.to(device)
     C = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), device=device)
-    if tune and stages == 0 and R is None:
+    if tune and stages == 0 and R is None and not w.b_coded:
         # the library's own tuner picks the configuration (outside the timed steps)
         sg.tune(A, B, epilogue=w.epilogue, bias=bias, out=C, stream=stream)
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def call():
-        sg.stage_gemm(A, B, epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream, residual=R)
+        if w.b_coded:
+            sg.stage_gemm_qb(A, B[0], B[1], epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream)
+        else:
+            sg.stage_gemm(A, B, epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream, residual=R)
 
     def flush():
         flush_buf.fill_(1)
@@ -477,6 +497,8 @@ def main():
     ms = sum_ms / len(times)
     value = whole_job_tflops(w.flops, world, len(times), sum_ms)
     plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages)
+    if w.b_coded:
+        plan["mode"] = 5  # mode 4's geometry with the panel decoded from int8 codes (stage_gemm_qb)
     plan["tuned"] = args.tune and args.stages == 0 and w.dist_r is None
 
     lib_ref = None
@@ -486,7 +508,7 @@ def main():
             lib_ref["ours_over_library"] = (w.flops / (ms * 1e-3) / 1e12) / lib_ref["value"]
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not w.b_coded:  # the host-buffer entry takes 16-bit or FP8 B only
         del dev_tensors
         e2e_ms, h2d, d2h = measure_e2e(sg, w, host_inputs, device, stream, max(3, min(args.steps, 10)), args.stages)
         e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
@@ -515,7 +537,7 @@ def main():
 
     if rank == 0 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD:
         sec = []
-        for name in ("relu4096_f16", "swin4k_proj_f16", "swin4k_backproj_f16", "square8192_e4m3"):
+        for name in ("relu4096_f16", "swin4k_proj_f16", "swin4k_backproj_f16", "square8192_e4m3", "swin4k_proj_i8w"):
             ws = gemm_inputs.WORKLOADS[name]
             t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=args.tune)
             m2 = sum(t2) / len(t2)

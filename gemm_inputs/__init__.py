@@ -150,6 +150,7 @@ class Workload:
     seed: int
     description: str
     dist_r: tuple | None = None   # residual R (M x N, output type), if the workload has one
+    b_coded: bool = False         # B given as int8 codes with one fp32 scale per column
 
     @property
     def flops(self) -> int:
@@ -160,7 +161,8 @@ class Workload:
         """Each operand read once and C written once (bias included)."""
         out_size = {"f32": 4, "f16": 2, "bf16": 2}[self.out_dtype]
         in_size = 1 if self.in_dtype == "e4m3" else 2
-        b = in_size * (self.M * self.K + self.K * self.N) + out_size * self.M * self.N
+        b_bytes = (self.K * self.N + 4 * self.N) if self.b_coded else in_size * self.K * self.N
+        b = in_size * self.M * self.K + b_bytes + out_size * self.M * self.N
         if self.epilogue == "bias_relu":
             b += 4 * self.N
         if self.dist_r is not None:
@@ -172,6 +174,17 @@ class Workload:
 
     def b_bits(self, ld: int | None = None) -> np.ndarray:
         return matrix_bits(self.seed, STREAM_B, self.K, self.N, self.dist_b, self.in_dtype, ld)
+
+    def b_codes(self) -> tuple[np.ndarray, np.ndarray]:
+        """B as int8 codes (K x N) and one fp32 scale per column: B's seeded
+        values quantised per column, symmetric over 127 levels each side
+        (s_j = max_k |w_kj| / 127, q_kj = w_kj / s_j rounded to nearest even),
+        the usual form of quantised weights."""
+        w = draw(self.seed, STREAM_B, self.K * self.N, self.dist_b).reshape(self.K, self.N)
+        amax = np.abs(w).max(axis=0)
+        s = (np.where(amax > 0, amax, 1.0) / 127.0).astype(np.float32)
+        q = np.clip(np.rint(w / s.astype(np.float64)), -127, 127).astype(np.int8)
+        return q, s
 
     def r_bits(self) -> np.ndarray | None:
         """The residual's bit patterns (M x N, the output's storage type)."""
@@ -218,6 +231,12 @@ WORKLOADS = {
         "skinny-N back-projection of the Swin MLP band on a 3840x2160 frame in 4x4 patches: M=518400 tokens, "
         "K=384 -> N=96, C = A.W + R with the residual R as the accumulator's seed, fp16 in/out",
         dist_r=("normal", 0.0, 1.0)),
+    "swin4k_proj_i8w": Workload(
+        "swin4k_proj_i8w", 518400, 384, 96, "f16", "f16", "bias_relu",
+        ("normal", 0.0, 1.0), ("normal", 0.0, 0.1), ("normal", 0.0, 0.1), 1008,
+        "the skinny-K token projection with int8-coded weights (per-column scales): M=518400 tokens, K=96 -> "
+        "N=384, C = relu(A.(Q.diag(s)) + b), fp16 activations and output, B decoded once per CTA into a "
+        "shared-memory panel", b_coded=True),
 }
 
 # The five workloads in the order they are listed for this path.

@@ -153,6 +153,31 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K,
                      const float* bias, int stages, void* stream);
 
 /*
+ * sg_gemm_qb -- C = epilogue(A . B) with an integer-coded B: Bq holds signed
+ * 8-bit codes q (K x N row-major, pitch ldb >= N, single bytes, no alignment
+ * rule) and b_scale one fp32 value s_j per column (device pointers), so
+ * that b_kj = s_j * q_kj; A is fp16 or bf16 (in_dtype) as for sg_gemm.  The
+ * pages' decoded panel (Tolk.Stage, "Decoded panels on the host": an operand
+ * decoded from integer codes, as a quantised matrix's is, has the values of
+ * its panel decoded once and read back by every trip of the other output
+ * loops) is taken on the GPU: each CTA decodes all of B once into shared
+ * memory as 16-bit values equal to the codes (exact), every row tile's MMAs
+ * read that panel, and s_j multiplies column j of the fp32 accumulator
+ * before the bias and the ReLU.  B must fit the resident panel: K <= 128
+ * and N <= 512 (else SG_ERR_ARG), and A must be TMA-legal (16-byte aligned
+ * base, pitch a multiple of 16 bytes; else SG_ERR_ARG).  The scales must be
+ * finite.  C must not overlap A, Bq, b_scale or bias (SG_ERR_ALIAS); a NULL
+ * b_scale, or a NULL Bq with K > 0, is SG_ERR_ARG; in_dtype other than
+ * fp16/bf16 is SG_ERR_DTYPE.  Everything else is as for sg_gemm.
+ */
+int sg_gemm_qb(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const int8_t* Bq, int64_t ldb, const float* b_scale,
+               void* C, int64_t ldc,
+               int in_dtype, int out_dtype, int epilogue,
+               const float* bias, int stages, void* stream);
+
+/*
  * sg_gemm_host -- the same product, C = epilogue(A . B [+ R]), on HOST
  * buffers: A, B, R (may be NULL: no residual), bias and C are host pointers
  * with the meanings, layouts and pitches of sg_gemm / sg_gemm_residual.

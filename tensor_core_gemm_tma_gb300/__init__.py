@@ -70,6 +70,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.sg_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
         lib.sg_gemm_residual.restype = i32
         lib.sg_gemm_residual.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
+        lib.sg_gemm_qb.restype = i32
+        lib.sg_gemm_qb.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, vp, i64, i32, i32, i32, vp, i32, vp]
         lib.sg_gemm_host.restype = i32
         lib.sg_gemm_host.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
         lib.sg_plan.restype = i32
@@ -192,6 +194,44 @@ def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: 
         rc = gemm_raw(M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), out.data_ptr(),
                       _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype), EPILOGUES[epilogue], bptr,
                       int(stages), _stream_ptr(stream, A.device).value)
+    _check(rc)
+    return out
+
+
+def stage_gemm_qb(A, Bq, b_scale, out_dtype=None, epilogue: str = "none", bias=None, stages: int = 0, out=None,
+                  stream=None):
+    """C = epilogue(A @ (Bq * b_scale)) with an integer-coded B: ``Bq`` an
+    int8 CUDA tensor of codes (K x N, K <= 128, N <= 512), ``b_scale`` an
+    fp32 CUDA vector of N per-column scales; A fp16 or bf16.  Each CTA
+    decodes B once into shared memory and every row tile reads it back."""
+    torch = _torch()
+    if A.device.type != "cuda" or Bq.device.type != "cuda" or b_scale.device.type != "cuda":
+        raise ValueError("A, Bq and b_scale must be CUDA tensors")
+    if Bq.dtype != torch.int8:
+        raise ValueError("Bq must hold int8 codes")
+    M, K = A.shape
+    K2, N = Bq.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if b_scale.dtype != torch.float32 or b_scale.numel() != N or not b_scale.is_contiguous():
+        raise ValueError("b_scale must be a contiguous fp32 vector of N values")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    elif out_dtype is not None and out.dtype != out_dtype:
+        raise ValueError("out has a different dtype from out_dtype")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be M x N")
+    if epilogue not in EPILOGUES:
+        raise ValueError(f"epilogue must be one of {sorted(EPILOGUES)}")
+    bptr = None
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.device != A.device or bias.numel() != N or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous fp32 CUDA vector of N values")
+        bptr = bias.data_ptr()
+    rc = load_library().sg_gemm_qb(M, N, K, A.data_ptr(), _row_pitch(A), Bq.data_ptr(), _row_pitch(Bq),
+                                   b_scale.data_ptr(), out.data_ptr(), _row_pitch(out), dtype_code(A.dtype),
+                                   dtype_code(out.dtype), EPILOGUES[epilogue], bptr, int(stages),
+                                   _stream_ptr(stream, A.device).value)
     _check(rc)
     return out
 

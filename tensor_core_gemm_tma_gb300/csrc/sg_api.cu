@@ -42,8 +42,8 @@ struct DevState {
     int major = 0, minor = 0;
     int* status = nullptr;  // device status word (4 bytes, library-owned)
     // per kernel instantiation [tile width][output type][mode - 1][residual]:
-    bool attr_done[2][3][3][4][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
-    int max_clusters[2][3][3][4][2] = {};  // the same index: co-resident clusters (0: not queried)
+    bool attr_done[2][3][3][5][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
+    int max_clusters[2][3][3][5][2] = {};  // the same index: co-resident clusters (0: not queried)
     // sg_gemm_host: library-owned copy streams, a second compute stream and
     // events, created on first use
     cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
@@ -276,7 +276,8 @@ std::atomic<int> g_force_mode{[] {
 }()};
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, const void* C,
-              int64_t ldc, int stages, bool a_tma, bool b_tma, Plan* pl, const Choice* choice = nullptr) {
+              int64_t ldc, int stages, bool a_tma, bool b_tma, Plan* pl, const Choice* choice = nullptr,
+              bool decode = false) {
     const int esz = elem_bytes(in_dtype);
     const int boxc = 128 / esz;  // B columns per 128-byte box: tile widths and CTA shares are multiples
     pl->a_tma = a_tma ? 1 : 0;
@@ -328,7 +329,15 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     if (const int f = g_force_mode.load(); f && legal(f)) mode = f;
     if (choice && choice->mode && legal(choice->mode)) mode = choice->mode;
     if (!a_tma || !b_tma) mode = 1;  // element-load staging runs in single-CTA mode
-    if (mode == 4) {
+    if (decode) {
+        // mode 5: the integer-coded B is decoded into mode 4's resident panel,
+        // so B must fit there (it is never read by TMA)
+        if (!(a_tma && pl->k_chunks <= 2 && nb128 <= 4 && smem_panel(128, 2, pl->k_chunks, nb128) <= st.smem_optin))
+            return SG_ERR_ARG;
+        mode = 5;
+    }
+    const bool panel = mode == 4 || mode == 5;
+    if (panel) {
         bn = 128;
         pl->bn = bn;
         pl->n_blocks = nb128;
@@ -337,11 +346,11 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     pl->cm = (mode == 2 || mode == 3) ? 2 : 1;
     const int cm = pl->cm;
     // work units handed out by the persistent loop: cluster tiles (modes 1-3)
-    // or row tiles covering every column block (mode 4)
-    pl->tiles = mode == 4 ? pl->m_blocks : cdiv(pl->m_blocks, cm) * pl->n_blocks;
+    // or row tiles covering every column block (modes 4, 5)
+    pl->tiles = panel ? pl->m_blocks : cdiv(pl->m_blocks, cm) * pl->n_blocks;
     int maxs = 0;
     for (int s = 1; s <= SG_MAX_STAGES; ++s) {
-        const int64_t need = mode == 4 ? smem_panel(bn, s, pl->k_chunks, pl->n_blocks) : smem_for(bn, s, mode);
+        const int64_t need = panel ? smem_panel(bn, s, pl->k_chunks, pl->n_blocks) : smem_for(bn, s, mode);
         if (need <= st.smem_optin) maxs = s;
     }
     pl->max_stages = maxs;
@@ -350,8 +359,8 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     if (stages == 0) stages = maxs;
     if (stages > maxs) return SG_ERR_STAGES;
     pl->stages = stages;
-    pl->smem = mode == 4 ? static_cast<int>(smem_panel(bn, stages, pl->k_chunks, pl->n_blocks))
-                         : smem_for(bn, stages, mode);
+    pl->smem = panel ? static_cast<int>(smem_panel(bn, stages, pl->k_chunks, pl->n_blocks))
+                     : smem_for(bn, stages, mode);
     pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for
     // it; keep one persistent CTA per SM by asking for more than half of the
@@ -394,7 +403,9 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
                 const CUtensorMap& tc, const CUtensorMap& tr, const sg::Params& prm, bool residual,
                 cudaStream_t stream) {
     sg::LaunchFn fn = nullptr;
-    if (pl.mode == 4)
+    if (pl.mode == 5)
+        fn = sg::launcher_decoded(out_dtype);
+    else if (pl.mode == 4)
         fn = sg::launcher_panel(out_dtype, residual, pl.block_k == sg::BK_BYTES ? 1 : 2);
     else if (pl.block_k == sg::BK_BYTES)  // 8-bit operands
         fn = residual ? sg::launcher_fp8_res(pl.bn, out_dtype, pl.mode) : sg::launcher_fp8_plain(pl.bn, out_dtype, pl.mode);
@@ -422,8 +433,6 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
     return fn(a) == 0 ? SG_OK : SG_ERR_CUDA;
 }
 
-// Plan, build the tensor maps and kernel parameters, and launch (shared by
-// both entry points; `st` supplies the device's attributes and status word).
 void fill_info(const Plan& pl, sg_plan_info* info) {
     std::memset(info, 0, sizeof(*info));
     info->block_m = sg::BM;
@@ -463,20 +472,26 @@ bool lookup_tuned(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, 
     return true;
 }
 
+// Plan, build the tensor maps and kernel parameters, and launch (shared by
+// the entry points; `st` supplies the device's attributes and status word).
+// With Bq (mode 5) B is int8 codes with per-column scales b_scale, decoded
+// into the resident panel; B is then unused.
 int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
                     int stages, int64_t skip_load, cudaStream_t stream, const Choice* forced = nullptr,
-                    Plan* used = nullptr, const void* R = nullptr, int64_t ldr = 0) {
+                    Plan* used = nullptr, const void* R = nullptr, int64_t ldr = 0, const int8_t* Bq = nullptr,
+                    const float* b_scale = nullptr) {
     const int esz = elem_bytes(in_dtype);
-    const bool a_tma = tma_legal(A, M, lda, esz);
-    const bool b_tma = tma_legal(B, K, ldb, esz);
+    const bool decode = Bq != nullptr;
+    const bool a_tma = (decode && K == 0) || tma_legal(A, M, lda, esz);  // mode 5 with K = 0 reads no A
+    const bool b_tma = decode || tma_legal(B, K, ldb, esz);
     Choice tuned;
     const Choice* choice = forced;
-    if (!choice && lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, a_tma, b_tma,
-                                c_tma_legal(C, M, ldc, out_dtype), &tuned))
+    if (!choice && !decode &&
+        lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, a_tma, b_tma, c_tma_legal(C, M, ldc, out_dtype), &tuned))
         choice = &tuned;
     Plan pl;
-    int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice);
+    int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice, decode);
     if (rc != SG_OK) return rc;
     if (used) *used = pl;
 
@@ -488,7 +503,7 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     if (K > 0) {
         const uint32_t kb = sg::BK_BYTES / esz, boxc = 128 / esz;
         if (a_tma && (rc = encode_2d(&ta, in_dtype, A, K, M, lda * esz, kb, sg::BM)) != SG_OK) return rc;
-        if (b_tma && (rc = encode_2d(&tb, in_dtype, B, N, K, ldb * esz, boxc, kb)) != SG_OK) return rc;
+        if (!decode && b_tma && (rc = encode_2d(&tb, in_dtype, B, N, K, ldb * esz, boxc, kb)) != SG_OK) return rc;
     }
     const int oes = elem_bytes(out_dtype);
     if (pl.tma_store) {
@@ -529,6 +544,9 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.R = R;
     prm.ldr = ldr;
     prm.r_tma = r_tma ? 1 : 0;
+    prm.Bq = Bq;
+    prm.b_scale = b_scale;
+    prm.in_bf16 = in_dtype == SG_BF16 ? 1 : 0;
     return launch_plan(st, out_dtype, pl, ta, tb, tc, tr, prm, R != nullptr, stream);
 }
 
@@ -564,6 +582,29 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
     if ((rc = device_state(&st)) != SG_OK) return rc;
     return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
                            g_skip_load.load(), static_cast<cudaStream_t>(stream), nullptr, nullptr, R, ldr);
+}
+
+int sg_gemm_qb(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const int8_t* Bq, int64_t ldb,
+               const float* b_scale, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue,
+               const float* bias, int stages, void* stream) {
+    if (in_dtype != SG_F16 && in_dtype != SG_BF16) return SG_ERR_DTYPE;
+    // A's checks (B's are taken below: its elements are single bytes)
+    int rc = check_args(M, N, K, A, lda, A, N, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    if (!b_scale || ldb > 0x7FFFFFFF) return SG_ERR_ARG;
+    if (K > 0 && (!Bq || ldb < N)) return SG_ERR_ARG;
+    const uint64_t c_span = span_bytes(M, N, ldc, elem_bytes(out_dtype));
+    if ((K > 0 && overlap(C, c_span, Bq, span_bytes(K, N, ldb, 1))) ||
+        overlap(C, c_span, b_scale, static_cast<uint64_t>(N) * 4))
+        return SG_ERR_ALIAS;
+    DevState* st = nullptr;
+    if ((rc = device_state(&st)) != SG_OK) return rc;
+    // a K = 0 product reads no codes: any non-null pointer marks the mode
+    const int8_t* codes = K > 0 ? Bq : reinterpret_cast<const int8_t*>(b_scale);
+    return plan_and_launch(*st, M, N, K, A, lda, nullptr, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                           g_skip_load.load(), static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, 0, codes,
+                           b_scale);
 }
 
 int sg_gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -148,6 +148,12 @@ struct Params {
     const void* R;
     int64_t ldr;
     int32_t r_tma;         // 1: R tiles are loaded by TMA, 0: by element loads
+    // Mode 5: B given as int8 codes (K x N, pitch ldb) with one fp32 scale
+    // per column; decoded into the resident panel as the operands' 16-bit
+    // type (bf16 when in_bf16), the scale applied to the accumulator.
+    const int8_t* Bq;
+    const float* b_scale;
+    int32_t in_bf16;
 };
 
 template <int ESZ>
@@ -362,6 +368,107 @@ __device__ __forceinline__ void store_one(void* C, int64_t idx, float v) {
     }
 }
 
+// Mode 5: one warp's share of decoding the integer-coded B into the
+// resident panel.  The panel has the layout TMA gives a 16-bit B: K chunk
+// kc and column block nb (of 128 columns) at (kc * n_blocks + nb) *
+// block_bytes, 64-column box j of it at j * box_bytes, K row r of the box at
+// r * 128 bytes, and its 16-byte chunk c (8 columns) at position c ^ (r mod
+// 8) (the 128-byte swizzle).  A code becomes the 16-bit value equal to it
+// (exact: |code| <= 128); codes past K or N are written as 0, the zero fill
+// of a TMA load.  Warp `part` of `nparts` takes every nparts-th group of 32
+// chunks.  The panel is decoded before any MMA can start, so each lane
+// issues the loads of DEC_UNROLL chunks (8 codes each: one 8-byte load when
+// the codes are 8-byte aligned) before it converts any of them.
+constexpr int DEC_UNROLL = 16;
+__device__ __forceinline__ void decode_panel(uint32_t panel, const Params& p, int n_blocks, int k_chunks,
+                                             uint32_t block_bytes, uint32_t box_bytes, int part, int nparts,
+                                             int lane) {
+    const int chunks = n_blocks * 16;  // 16-byte chunks in one K row of the panel
+    const int total = k_chunks * 64 * chunks;
+    const int step = nparts * 32;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.Bq) | static_cast<uintptr_t>(p.ldb)) & 7) == 0;
+    for (int t0 = part * 32 + lane; t0 < total; t0 += step * DEC_UNROLL) {
+        uint2 codes[DEC_UNROLL];
+#pragma unroll
+        for (int u = 0; u < DEC_UNROLL; ++u) {
+            const int t = t0 + u * step;
+            const int k = t / chunks, n0 = (t % chunks) * 8;
+            codes[u] = make_uint2(0u, 0u);
+            if (t < total && k < p.K && n0 < p.N) {
+                const int8_t* src = p.Bq + static_cast<int64_t>(k) * p.ldb + n0;
+                if (vec && n0 + 8 <= p.N) {
+                    codes[u] = __ldg(reinterpret_cast<const uint2*>(src));
+                } else {
+                    uint32_t lo = 0, hi = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t byte = (n0 + i < p.N) ? static_cast<uint8_t>(__ldg(src + i)) : 0u;
+                        if (i < 4) lo |= byte << (8 * i);
+                        else hi |= byte << (8 * (i - 4));
+                    }
+                    codes[u] = make_uint2(lo, hi);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < DEC_UNROLL; ++u) {
+            const int t = t0 + u * step;
+            if (t >= total) break;
+            const int k = t / chunks, n0 = (t % chunks) * 8;
+            const int kc = k >> 6, r = k & 63, nb = n0 >> 7, col = n0 & 127;
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t word = h < 2 ? codes[u].x : codes[u].y;
+                const int sh = 16 * (h & 1);
+                const float lo = static_cast<float>(static_cast<int8_t>((word >> sh) & 0xFFu));
+                const float hi = static_cast<float>(static_cast<int8_t>((word >> (sh + 8)) & 0xFFu));
+                if (p.in_bf16) {
+                    __nv_bfloat162 x = __floats2bfloat162_rn(lo, hi);
+                    w[h] = *reinterpret_cast<uint32_t*>(&x);
+                } else {
+                    __half2 x = __floats2half2_rn(lo, hi);
+                    w[h] = *reinterpret_cast<uint32_t*>(&x);
+                }
+            }
+            const uint32_t c = static_cast<uint32_t>((col & 63) >> 3);
+            st_shared_v4(panel + static_cast<uint32_t>(kc * n_blocks + nb) * block_bytes + (col >> 6) * box_bytes +
+                             r * 128 + ((c ^ static_cast<uint32_t>(r & 7)) << 4),
+                         w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// v * scale[col] (+ bias[col] when bias is given) for the COLS columns
+// starting at col0: mode 5's per-column scale of the integer-coded B, fused
+// with the bias into one multiply-add per element (each rounded once, as
+// the separate multiply and add would not be: the scaled sum is exact in
+// neither, and the tolerance covers both).  Nothing past N.
+template <int COLS>
+__device__ __forceinline__ void scale_bias(float (&v)[COLS], const float* __restrict__ scale,
+                                           const float* __restrict__ bias, int col0, int N) {
+    const uintptr_t bb = bias ? reinterpret_cast<uintptr_t>(bias + col0) : 0;
+    if (col0 + COLS <= N && ((reinterpret_cast<uintptr_t>(scale + col0) | bb) & 15) == 0) {
+        const float4* s4 = reinterpret_cast<const float4*>(scale + col0);
+        const float4* b4 = reinterpret_cast<const float4*>(bb);
+#pragma unroll
+        for (int i = 0; i < COLS / 4; ++i) {
+            const float4 sc = __ldg(s4 + i);
+            const float4 b = bias ? __ldg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * i + 0] = fmaf(v[4 * i + 0], sc.x, b.x);
+            v[4 * i + 1] = fmaf(v[4 * i + 1], sc.y, b.y);
+            v[4 * i + 2] = fmaf(v[4 * i + 2], sc.z, b.z);
+            v[4 * i + 3] = fmaf(v[4 * i + 3], sc.w, b.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < COLS; ++i) {
+            const int col = col0 + i;
+            if (col < N) v[i] = fmaf(v[i], __ldg(scale + col), bias ? __ldg(bias + col) : 0.0f);
+        }
+    }
+}
+
 // + bias[col] for the COLS columns starting at col0 (zero past N).
 template <int COLS>
 __device__ __forceinline__ void add_bias(float (&v)[COLS], const float* __restrict__ bias, int col0, int N) {
@@ -393,9 +500,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const Params p) {
-    static_assert(MODE >= 1 && MODE <= 4, "mode 1, 2, 3 or 4");
+    static_assert(MODE >= 1 && MODE <= 5, "mode 1 to 5");
     constexpr int CM = (MODE == 2 || MODE == 3) ? 2 : 1;  // CTAs per cluster
-    constexpr bool PANEL = (MODE == 4);        // B resident in shared memory
+    constexpr bool PANEL = (MODE == 4 || MODE == 5);      // B resident in shared memory
+    constexpr bool DECODE = (MODE == 5);                  // ... decoded there from int8 codes
+    static_assert(!DECODE || (ESZ == 2 && !RES), "mode 5: 16-bit A, no residual");
     constexpr bool PAIR = (MODE == 3);         // paired MMA (cta_group::2)
     constexpr int CG = PAIR ? 2 : 1;           // cta_group of every tcgen05 instruction
     constexpr int BL = PAIR ? BN / 2 : BN;     // B columns staged by this CTA
@@ -416,9 +525,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t base = (raw + SMEM_ALIGN - 1) & ~static_cast<uint32_t>(SMEM_ALIGN - 1);
     uint8_t* gbase = smem_raw + (base - raw);
     const int stages = p.stages;
-    // Shared-memory map.  Modes 1-3: [ring][staging][barriers].  Mode 4:
-    // [resident B: k_chunks x n_blocks blocks of BN columns][ring of A tiles,
-    // each k_chunks A chunks][staging][barriers].
+    // Shared-memory map.  Modes 1-3: [ring][staging][barriers].  Modes 4
+    // and 5: [resident B: k_chunks x n_blocks blocks of BN columns][ring of A
+    // tiles, each k_chunks A chunks][staging][barriers].
     constexpr int B_BLOCK_BYTES = (BN / G::BOXC) * G::B_BOX_BYTES;  // one K chunk of one column block
     const uint32_t res_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks * p.n_blocks) * B_BLOCK_BYTES : 0u;
     const uint32_t stage_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks) * A_STAGE_BYTES : L::STAGE_BYTES;
@@ -453,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(drain_bar, 1);
         for (int e = 0; e < EPI_WARPS; ++e) mbar_init(rres_bar(e), 1);
-        mbar_init(bres_bar, 1);
+        mbar_init(bres_bar, DECODE ? EPI_WARPS : 1);  // mode 5: every epilogue warp decodes a share
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -538,7 +647,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued = 0, last_parity = 0;  // per slot: ever filled, parity of its last fill
             int64_t it = 0;
             bool ok = true;
-            if constexpr (PANEL) {
+            if constexpr (PANEL && !DECODE) {
                 // the resident B: every K chunk of every column block, once
                 mbar_arrive_expect_tx(bres_bar, res_bytes);
                 for (int kc = 0; kc < p.k_chunks; ++kc)
@@ -601,7 +710,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // even CTA's barriers also count the odd CTA's copies)
                 for (int s = 0; s < stages; ++s)
                     if ((issued >> s) & 1u) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
-                if (PANEL) wait_drain(bres_bar, 0, p.wait_limit_ns);
+                if (PANEL && !DECODE) wait_drain(bres_bar, 0, p.wait_limit_ns);
             }
         }
     } else if (warp == 1) {
@@ -756,8 +865,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             r_pending = true;
         };
+        if constexpr (DECODE) {
+            // the panel is decoded once and read back by the MMAs of every row tile
+            decode_panel(base, p, p.n_blocks, p.k_chunks, B_BLOCK_BYTES, G::B_BOX_BYTES, e, EPI_WARPS, lane);
+            fence_proxy_async_smem();  // the MMA reads it through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bres_bar);
+        }
         uint32_t ab = 0, aph = 0;
-        // units: one per tile (modes 1-3), or (row tile, column block) pairs (mode 4)
+        // units: one per tile (modes 1-3), or (row tile, column block) pairs (modes 4, 5)
         const int subs = PANEL ? p.n_blocks : 1;
         for (int tile = cluster_id, sub = 0; tile < p.num_tiles;) {
             int mb = tile, nb = sub;
@@ -814,7 +930,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
-                if (p.epi == SG_EPI_BIAS_RELU) add_bias<COLS>(v, p.bias, col0, p.N);
+                if constexpr (DECODE) {
+                    scale_bias<COLS>(v, p.b_scale, p.epi == SG_EPI_BIAS_RELU ? p.bias : nullptr, col0, p.N);
+                } else if (p.epi == SG_EPI_BIAS_RELU) {
+                    add_bias<COLS>(v, p.bias, col0, p.N);
+                }
                 const bool relu = p.epi != SG_EPI_NONE;
                 if (OUT == SG_F32 || !p.tma_store) {
                     if (relu) {

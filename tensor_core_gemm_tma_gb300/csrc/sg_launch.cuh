@@ -87,5 +87,6 @@ LaunchFn launcher_fp8_plain(int bn, int out, int mode);
 LaunchFn launcher_fp8_res(int bn, int out, int mode);
 // Mode 4 (resident B), tile width 128, either element size (esz 1 or 2):
 LaunchFn launcher_panel(int out, bool residual, int esz);
+LaunchFn launcher_decoded(int out);  // mode 5: 16-bit A, int8-coded B decoded into the resident panel
 
 }  // namespace sg
