@@ -1,6 +1,7 @@
 // sg_kernel.cuh -- the persistent, warp-specialised sm_103a GEMM kernel
 //
-//     C = epilogue(A . B),  A: M x K row-major, B: K x N row-major (fp16/bf16),
+//     C = epilogue(A . B [+ R]),  A: M x K row-major, B: K x N row-major
+//     (fp16/bf16/FP8 E4M3, or int8 codes with per-column scales in mode 5),
 //     fp32 accumulation in tensor memory, C fp32 / fp16 / bf16.
 //
 // Roles (one CTA per SM, 320 threads):
@@ -11,11 +12,12 @@
 //               the "gate that copies 0 where it fails" of Tolk.Stage
 //               ("operands") and the "elements past the edge read 0" of
 //               gizml:tile ("In.at").
-//   warp 1      allocates tensor memory; one lane issues tcgen05.mma for each
-//               filled slot into a 128 x BN fp32 accumulator and frees the
-//               slot with tcgen05.commit.  512 / BN accumulators rotate, so
-//               the epilogue of earlier tiles overlaps the main loop of the
-//               next.
+//   warp 1      allocates tensor memory; the whole warp runs the loop (its
+//               slot, phase and descriptor values stay warp-uniform) and lane
+//               0 issues tcgen05.mma for each filled slot into a 128 x BN
+//               fp32 accumulator and frees the slot with tcgen05.commit.
+//               512 / BN (at most 4) accumulators rotate, so the epilogue of
+//               earlier tiles overlaps the main loop of the next.
 //   warps 2-9   epilogue: two warps per 32-lane quarter of tensor memory
 //               (a warp may only read the quarter given by its index mod 4),
 //               each taking every other 128-byte-wide column chunk:
@@ -24,7 +26,7 @@
 //               TMA store that does not write elements outside M x N
 //               (gizml:tile, "Out.put").
 //
-// Three modes (MODE):
+// Five modes (MODE):
 //   1  one CTA per 128 x BN tile.
 //   2  clusters of two CTAs with vertically adjacent 128 x BN tiles and the
 //      same column block: each CTA copies half of the B tile's 64-column
@@ -46,6 +48,13 @@
 //      its commits free the ring slots and hand accumulators to the
 //      epilogues of both CTAs; both epilogues release accumulators on the
 //      even CTA's barrier.
+//   5  decoded panel: mode 4 with B given as int8 codes and one fp32 scale
+//      per column.  At CTA start the eight epilogue warps decode all of B
+//      into the resident panel, each code to the 16-bit value equal to it,
+//      in the layout TMA would give (Tolk.Stage, "Decoded panels on the
+//      host": the panel is decoded once and read back by every trip of the
+//      other output loop); the epilogue multiplies by the column's scale,
+//      fused with the bias.
 //
 // The ring generalises the two-slot pipeline of Tolk.Stage (copy chunk k+1
 // into slot (k+1) mod 2 while computing on slot k mod 2) and the `stages`
