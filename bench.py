@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -82,12 +83,18 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources with comments and whitespace removed, so that
+    it changes only when the compiled code can."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_core_gemm_tma_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name)) as f:
+                code = f.read()
+            code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)           # block comments
+            code = re.sub(r'//[^\n]*', " ", code)                            # line comments
+            code = "".join(code.split())
+            h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
