@@ -568,6 +568,25 @@ def main():
                 entry["library_reference"] = lr
             del dt
             sec.append(entry)
+            if name == "relu4096_f16":
+                # the same product with the pages' tiling (a workgroup per 128 x 128
+                # output tile, gizml:tile's fused example): forced through the
+                # testing hooks; every tiling computes the same bits
+                lib = sg.load_library()
+                lib.sg_test_set_tile_n(128)
+                lib.sg_test_set_cluster(1)
+                try:
+                    t3, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=False)
+                    p3 = sg.plan(ws.M, ws.N, ws.K, torch.float16, torch.float16, ws.epilogue)
+                finally:
+                    lib.sg_test_set_tile_n(0)
+                    lib.sg_test_set_cluster(0)
+                del dt
+                m3 = sum(t3) / len(t3)
+                sec.append({"workload": name, "tiling": f"{p3['block_m']}x{p3['block_n']} single-CTA tiles "
+                                                        "(the pages' 128 x 128 output tile)",
+                            "ms_per_step": m3, "TFLOP/s": ws.flops / (m3 * 1e-3) / 1e12,
+                            "roofline": roofline_of(ws, m3, peaks, None)})
         line["secondary"] = sec
 
     if rank == 0 and not args.no_cpu_baseline and world >= 1:
