@@ -66,7 +66,10 @@ def _sampled_workload(name, n_random=4096, edge_rows=(), edge_cols=()):
 
 
 def test_square8192_bf16_sampled():
-    _sampled_workload("square8192_bf16", edge_rows=(0, 8191), edge_cols=(0, 8191))
+    # 4096 random elements, row 0 and column 0, and every element of the last
+    # row tile and the last column tile (256 = one paired tile's rows and columns)
+    edge = (0,) + tuple(range(8192 - 256, 8192))
+    _sampled_workload("square8192_bf16", edge_rows=edge, edge_cols=edge)
 
 
 def test_swin4k_proj_f16_sampled():
