@@ -58,6 +58,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     """Load libstage_gemm.so (built by ``__graft_entry__.build()`` or
     ``tensor_core_gemm_tma_gb300._build.build()``).  Raises if it is absent."""
     global _lib
+    if _lib is not None and path is None:  # the loaded library: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
@@ -118,18 +120,32 @@ def _torch():
     return torch
 
 
+_DTYPE_CODES = None
+
+
 def dtype_code(dt) -> int:
-    torch = _torch()
-    codes = {torch.float32: SG_F32, torch.float16: SG_F16, torch.bfloat16: SG_BF16}
-    if hasattr(torch, "float8_e4m3fn"):
-        codes[torch.float8_e4m3fn] = SG_E4M3
-    if dt not in codes:
+    global _DTYPE_CODES
+    if _DTYPE_CODES is None:
+        torch = _torch()
+        codes = {torch.float32: SG_F32, torch.float16: SG_F16, torch.bfloat16: SG_BF16}
+        if hasattr(torch, "float8_e4m3fn"):
+            codes[torch.float8_e4m3fn] = SG_E4M3
+        _DTYPE_CODES = codes
+    code = _DTYPE_CODES.get(dt)
+    if code is None:
         raise ValueError(f"unsupported dtype {dt}")
-    return codes[dt]
+    return code
 
 
 def _stream_ptr(stream, device):
     torch = _torch()
+    if stream is None:
+        # the current stream's handle without building a Stream object (the
+        # slowest part of a small call); the public route otherwise
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            idx = device.index if getattr(device, "index", None) is not None else torch.cuda.current_device()
+            return ctypes.c_void_p(raw(idx))
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
 
