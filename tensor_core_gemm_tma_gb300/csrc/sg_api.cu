@@ -231,12 +231,13 @@ struct Plan {
     int a_tma = 1, b_tma = 1;  // operand copied by TMA (1) or by element loads (0)
 };
 
-// Mode 4's shared memory: the resident B (k_chunks x n_blocks blocks of
-// bn columns by 128 bytes of K), a ring of A tiles (k_chunks chunks each),
-// the staging buffers and the barriers.
-int64_t smem_panel(int bn, int stages, int64_t k_chunks, int64_t n_blocks) {
+// Modes 4 and 5's shared memory: the resident B (k_chunks x n_blocks blocks
+// of bn columns by 128 bytes of K), a ring of A tiles (k_chunks chunks
+// each), the staging buffers, mode 5's per-column scales and biases (fp32,
+// n_blocks * bn of each) and the barriers.
+int64_t smem_panel(int bn, int stages, int64_t k_chunks, int64_t n_blocks, bool decode = false) {
     return k_chunks * n_blocks * bn * sg::BK_BYTES + stages * k_chunks * sg::A_STAGE_BYTES +
-           sg::EPI_WARPS * sg::EPI_BUF_BYTES + sg::BAR_AREA + sg::SMEM_ALIGN;
+           sg::EPI_WARPS * sg::EPI_BUF_BYTES + (decode ? n_blocks * bn * 8 : 0) + sg::BAR_AREA + sg::SMEM_ALIGN;
 }
 
 int smem_for(int bn, int stages, int mode) {
@@ -332,7 +333,8 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     if (decode) {
         // mode 5: the integer-coded B is decoded into mode 4's resident panel,
         // so B must fit there (it is never read by TMA)
-        if (!(a_tma && pl->k_chunks <= 2 && nb128 <= 4 && smem_panel(128, 2, pl->k_chunks, nb128) <= st.smem_optin))
+        if (!(a_tma && pl->k_chunks <= 2 && nb128 <= 4 &&
+              smem_panel(128, 1, pl->k_chunks, nb128, true) <= st.smem_optin))
             return SG_ERR_ARG;
         mode = 5;
     }
@@ -350,7 +352,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     pl->tiles = panel ? pl->m_blocks : cdiv(pl->m_blocks, cm) * pl->n_blocks;
     int maxs = 0;
     for (int s = 1; s <= SG_MAX_STAGES; ++s) {
-        const int64_t need = panel ? smem_panel(bn, s, pl->k_chunks, pl->n_blocks) : smem_for(bn, s, mode);
+        const int64_t need = panel ? smem_panel(bn, s, pl->k_chunks, pl->n_blocks, mode == 5) : smem_for(bn, s, mode);
         if (need <= st.smem_optin) maxs = s;
     }
     pl->max_stages = maxs;
@@ -359,7 +361,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     if (stages == 0) stages = maxs;
     if (stages > maxs) return SG_ERR_STAGES;
     pl->stages = stages;
-    pl->smem = panel ? static_cast<int>(smem_panel(bn, stages, pl->k_chunks, pl->n_blocks))
+    pl->smem = panel ? static_cast<int>(smem_panel(bn, stages, pl->k_chunks, pl->n_blocks, mode == 5))
                      : smem_for(bn, stages, mode);
     pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for

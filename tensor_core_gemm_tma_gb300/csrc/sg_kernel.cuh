@@ -448,33 +448,25 @@ __device__ __forceinline__ void decode_panel(uint32_t panel, const Params& p, in
     }
 }
 
-// v * scale[col] (+ bias[col] when bias is given) for the COLS columns
-// starting at col0: mode 5's per-column scale of the integer-coded B, fused
-// with the bias into one multiply-add per element (each rounded once, as
-// the separate multiply and add would not be: the scaled sum is exact in
-// neither, and the tolerance covers both).  Nothing past N.
+// Mode 5: v * scale[col] + bias[col] for the COLS columns starting at col0,
+// one multiply-add per element (each rounded once; the tolerance covers
+// it), with the scales at par + 4 * col and the biases (zeros without a
+// bias) at par + nbias + 4 * col in shared memory, copied there once per
+// CTA and zero past N.  Every lane reads the same addresses (broadcast).
 template <int COLS>
-__device__ __forceinline__ void scale_bias(float (&v)[COLS], const float* __restrict__ scale,
-                                           const float* __restrict__ bias, int col0, int N) {
-    const uintptr_t bb = bias ? reinterpret_cast<uintptr_t>(bias + col0) : 0;
-    if (col0 + COLS <= N && ((reinterpret_cast<uintptr_t>(scale + col0) | bb) & 15) == 0) {
-        const float4* s4 = reinterpret_cast<const float4*>(scale + col0);
-        const float4* b4 = reinterpret_cast<const float4*>(bb);
+__device__ __forceinline__ void scale_bias_smem(float (&v)[COLS], uint32_t par, uint32_t nbias, int col0) {
 #pragma unroll
-        for (int i = 0; i < COLS / 4; ++i) {
-            const float4 sc = __ldg(s4 + i);
-            const float4 b = bias ? __ldg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[4 * i + 0] = fmaf(v[4 * i + 0], sc.x, b.x);
-            v[4 * i + 1] = fmaf(v[4 * i + 1], sc.y, b.y);
-            v[4 * i + 2] = fmaf(v[4 * i + 2], sc.z, b.z);
-            v[4 * i + 3] = fmaf(v[4 * i + 3], sc.w, b.w);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < COLS; ++i) {
-            const int col = col0 + i;
-            if (col < N) v[i] = fmaf(v[i], __ldg(scale + col), bias ? __ldg(bias + col) : 0.0f);
-        }
+    for (int i = 0; i < COLS / 4; ++i) {
+        const uint32_t off = static_cast<uint32_t>(col0 + 4 * i) * 4u;
+        float s0, s1, s2, s3, b0, b1, b2, b3;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(s0), "=f"(s1), "=f"(s2), "=f"(s3) : "r"(par + off));
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b0), "=f"(b1), "=f"(b2), "=f"(b3)
+                     : "r"(par + nbias + off));
+        v[4 * i + 0] = fmaf(v[4 * i + 0], s0, b0);
+        v[4 * i + 1] = fmaf(v[4 * i + 1], s1, b1);
+        v[4 * i + 2] = fmaf(v[4 * i + 2], s2, b2);
+        v[4 * i + 3] = fmaf(v[4 * i + 3], s3, b3);
     }
 }
 
@@ -536,13 +528,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int stages = p.stages;
     // Shared-memory map.  Modes 1-3: [ring][staging][barriers].  Modes 4
     // and 5: [resident B: k_chunks x n_blocks blocks of BN columns][ring of A
-    // tiles, each k_chunks A chunks][staging][barriers].
+    // tiles, each k_chunks A chunks][staging][mode 5: scales, biases][barriers].
     constexpr int B_BLOCK_BYTES = (BN / G::BOXC) * G::B_BOX_BYTES;  // one K chunk of one column block
     const uint32_t res_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks * p.n_blocks) * B_BLOCK_BYTES : 0u;
     const uint32_t stage_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks) * A_STAGE_BYTES : L::STAGE_BYTES;
     const uint32_t ring0 = base + res_bytes;
     const uint32_t epi_off = res_bytes + static_cast<uint32_t>(stages) * stage_bytes;
-    const uint32_t bar_off = epi_off + EPI_WARPS * EPI_BUF_BYTES;
+    // mode 5: per-column scales then biases, fp32, n_blocks * BN of each
+    const uint32_t par_nbias = DECODE ? static_cast<uint32_t>(p.n_blocks) * BN * 4u : 0u;
+    const uint32_t par_off = epi_off + EPI_WARPS * EPI_BUF_BYTES;
+    const uint32_t bar_off = par_off + 2u * par_nbias;
 
     const uint32_t bar0 = base + bar_off;
     // barrier slots: full[0..7], empty[8..15], tmem_full[16..19], tmem_empty[20..23], drain[24],
@@ -880,6 +875,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();  // the MMA reads it through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(bres_bar);
+            // the per-column scales and biases, read by every chunk of every tile
+            const bool has_bias = p.epi == SG_EPI_BIAS_RELU;
+            for (int i = e * 32 + lane; i < p.n_blocks * BN; i += EPI_WARPS * 32) {
+                const float sc = i < p.N ? __ldg(p.b_scale + i) : 0.0f;
+                const float bi = (has_bias && i < p.N) ? __ldg(p.bias + i) : 0.0f;
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + par_off + 4u * i), "f"(sc) : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + par_off + par_nbias + 4u * i), "f"(bi) : "memory");
+            }
+            // all eight epilogue warps have written their share before any reads it
+            asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32) : "memory");
         }
         uint32_t ab = 0, aph = 0;
         // units: one per tile (modes 1-3), or (row tile, column block) pairs (modes 4, 5)
@@ -940,7 +945,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 if constexpr (DECODE) {
-                    scale_bias<COLS>(v, p.b_scale, p.epi == SG_EPI_BIAS_RELU ? p.bias : nullptr, col0, p.N);
+                    scale_bias_smem<COLS>(v, base + par_off, par_nbias, col0);
                 } else if (p.epi == SG_EPI_BIAS_RELU) {
                     add_bias<COLS>(v, p.bias, col0, p.N);
                 }
