@@ -42,3 +42,49 @@ def test_skipped_copy_times_out_and_context_survives(mode):
     got = run_gpu(a, b, M, N, K, "f16", "f32")
     ref, _, S = oracle.gemm(a, b, "f16", "f32")
     compare(got, ref, S, "f32", f"after-timeout mode {mode}")
+
+
+@pytest.mark.parametrize("coded", [False, True])
+def test_resident_panel_timeout_and_context_survives(coded):
+    """Modes 4 (resident B) and 5 (decoded panel): a skipped A copy (each CTA
+    has at least two row tiles, so its second fill exists) makes the MMA
+    issuer's wait run out; the CTA drains its copies (and, in mode 4, the
+    resident B's), SG_ERR_TIMEOUT is read, and the next call is correct."""
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = sg.load_library()
+    M, N, K = 40000, 384, 96                     # 313 row tiles over 152 CTAs
+    a, b = seeded_case(M, N, K, "f16", seed=32)
+    A = torch.from_numpy(a.view(np.int16)).cuda().view(torch.float16)
+    Bf = torch.from_numpy(b.view(np.int16)).cuda().view(torch.float16)
+    rng = np.random.default_rng(33)
+    q = rng.integers(-127, 128, (K, N), dtype=np.int16).astype(np.int8)
+    Q = torch.from_numpy(q).cuda()
+    S = torch.full((N,), 0.01, dtype=torch.float32, device="cuda")
+
+    def call():
+        return sg.stage_gemm_qb(A, Q, S) if coded else sg.stage_gemm(A, Bf)
+    old = sg.get_wait_limit_ns()
+    try:
+        assert lib.sg_test_set_cluster(0 if coded else 4) == 0
+        if not coded:
+            assert sg.plan(M, N, K, torch.float16, torch.float32)["mode"] == 4
+        sg.set_wait_limit_ns(50_000_000)          # 50 ms
+        lib.sg_test_set_skip_load(1)
+        call()
+        assert sg.device_status() == -8
+        assert sg.device_status() == 0
+    finally:
+        lib.sg_test_set_skip_load(-1)
+        sg.set_wait_limit_ns(old)
+        lib.sg_test_set_cluster(0)
+    C = call()
+    torch.cuda.synchronize()
+    assert sg.device_status() == 0
+    rows = np.arange(0, M, 97)
+    got = C.view(torch.int32).cpu().numpy().view(np.uint32)[rows]
+    if coded:
+        ref, _, Sx = oracle.gemm_qb(np.ascontiguousarray(a[rows]), q, np.full(N, 0.01, np.float32), "f16", "f32")
+    else:
+        ref, _, Sx = oracle.gemm(np.ascontiguousarray(a[rows]), b, "f16", "f32")
+    compare(got, ref, Sx, "f32", f"after-timeout {'mode 5' if coded else 'mode 4'}")
