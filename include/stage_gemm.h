@@ -234,8 +234,11 @@ typedef struct {
                               multicast) */
     int32_t group_m;       /* cluster row blocks swept together by the tile raster */
     int32_t mode;          /* 1 single CTA, 2 CTA pair sharing B by multicast,
-                              3 paired MMA, 4 B resident in shared memory */
-    int32_t reserved[1];
+                              3 paired MMA, 4 B resident in shared memory,
+                              5 integer-coded B decoded into shared memory */
+    int32_t ring_group;    /* ring slots filled and consumed together on one
+                              pair of barriers (2 when both operands arrive by
+                              TMA and the ring has 6 or 8 slots, else 1) */
 } sg_plan_info;
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,

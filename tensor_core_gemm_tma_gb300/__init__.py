@@ -44,10 +44,10 @@ class SgError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "block_n", "block_k", "stages", "max_stages", "tiles", "grid", "threads", "smem_bytes",
-        "tmem_columns", "tma_store", "cluster_m", "pair_mma", "group_m", "mode")] + [("reserved", ctypes.c_int32 * 1)]
+        "tmem_columns", "tma_store", "cluster_m", "pair_mma", "group_m", "mode", "ring_group")]
 
     def as_dict(self) -> dict:
-        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 _lock = threading.Lock()

@@ -59,9 +59,13 @@
 // The ring generalises the two-slot pipeline of Tolk.Stage (copy chunk k+1
 // into slot (k+1) mod 2 while computing on slot k mod 2) and the `stages`
 // knob of gizml:tile ("Program.stages") to S slots; full/empty mbarriers with
-// phase bits replace the workgroup barrier.  Every stage count issues the
-// same MMAs in the same K order, so C is bit-identical for all of them
-// (Tolk.Stage: staging moves values and never rounds them).
+// phase bits replace the workgroup barrier.  With 6 or 8 slots and both
+// operands copied by TMA, slots are filled and consumed in pairs on the
+// first slot's barriers (the MMA warp then waits once per two chunks; each
+// wait stalls its issue long enough for the tensor pipe to run dry).  Every
+// stage count issues the same MMAs in the same K order, so C is
+// bit-identical for all of them (Tolk.Stage: staging moves values and never
+// rounds them).
 //
 // Each warp's loop trip counts depend only on the problem size and the tile
 // index (Tolk.Uniform: barriers and matrix multiply-accumulates run under
@@ -135,6 +139,7 @@ struct Params {
     int32_t M, N, K;
     int32_t m_blocks, n_blocks, num_tiles, k_chunks;  // num_tiles counts cluster tiles (CM row blocks each)
     int32_t stages;
+    int32_t ring_group;    // ring slots filled and consumed together on one barrier pair (1 or 2)
     int32_t group_m;       // tile raster: group_m row-blocks swept together for L2 reuse
     uint32_t idesc;        // tcgen05 instruction descriptor
     int32_t epi;           // SG_EPI_*
@@ -526,6 +531,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t base = (raw + SMEM_ALIGN - 1) & ~static_cast<uint32_t>(SMEM_ALIGN - 1);
     uint8_t* gbase = smem_raw + (base - raw);
     const int stages = p.stages;
+    // slots per ring barrier pair; a group must divide the ring
+    const int ring_group = (p.ring_group == 2 && stages % 2 == 0 && p.a_tma && p.b_tma) ? 2 : 1;
     // Shared-memory map.  Modes 1-3: [ring][staging][barriers].  Modes 4
     // and 5: [resident B: k_chunks x n_blocks blocks of BN columns][ring of A
     // tiles, each k_chunks A chunks][staging][mode 5: scales, biases][barriers].
@@ -665,13 +672,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int mb = tile, nb = 0;
                 if constexpr (!PANEL) tile_coords<CM>(tile, p, rank, mb, nb);
                 const int fills = PANEL ? 1 : p.k_chunks;  // mode 4: one ring slot holds every K chunk of A
-                for (int kc = 0; kc < fills; ++kc, ++it) {
+                const int grp = PANEL ? 1 : ring_group;
+                for (int kc = 0; kc < fills; kc += grp, it += grp) {
                     if (!wait_bounded(empty_bar(slot), phase ^ 1u, abort_flag, p.status, p.wait_limit_ns,
                                       SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    if (it != p.skip_load) {
+                    const int nq = min(grp, fills - kc);  // K chunks in this group of slots
+                    if (p.skip_load < it || p.skip_load >= it + nq) {
                         const uint32_t sa = ring0 + slot * stage_bytes;
                         if constexpr (PANEL) {
                             mbar_arrive_expect_tx(full_bar(slot), stage_bytes);
@@ -680,30 +689,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         } else if constexpr (PAIR) {
                             // both CTAs' copies complete on the even CTA's barrier
                             const uint32_t fb = mapa_shared(full_bar(slot), 0);
-                            if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), 2 * L::STAGE_BYTES);
-                            tma_load_2d_pair(sa, &tmA, fb, kc * G::KB, mb * BM);
+                            if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), nq * 2 * L::STAGE_BYTES);
+                            for (int c = 0; c < nq; ++c) {
+                                const uint32_t sc = sa + c * stage_bytes;
+                                const int k0 = (kc + c) * G::KB;
+                                tma_load_2d_pair(sc, &tmA, fb, k0, mb * BM);
 #pragma unroll
-                            for (int j = 0; j < BL / G::BOXC; ++j)
-                                tma_load_2d_pair(sa + A_STAGE_BYTES + j * G::B_BOX_BYTES, &tmB, fb,
-                                                 nb * BN + static_cast<int>(rank) * BL + j * G::BOXC, kc * G::KB);
+                                for (int j = 0; j < BL / G::BOXC; ++j)
+                                    tma_load_2d_pair(sc + A_STAGE_BYTES + j * G::B_BOX_BYTES, &tmB, fb,
+                                                     nb * BN + static_cast<int>(rank) * BL + j * G::BOXC, k0);
+                            }
                         } else {
-                            mbar_arrive_expect_tx(full_bar(slot), L::STAGE_BYTES);
-                            tma_load_2d(sa, &tmA, full_bar(slot), kc * G::KB, mb * BM);
+                            mbar_arrive_expect_tx(full_bar(slot), nq * L::STAGE_BYTES);
+                            for (int c = 0; c < nq; ++c) {
+                                const uint32_t sc = sa + c * stage_bytes;
+                                const int k0 = (kc + c) * G::KB;
+                                tma_load_2d(sc, &tmA, full_bar(slot), k0, mb * BM);
 #pragma unroll
-                            for (int j = 0; j < BN / G::BOXC; ++j) {
-                                const uint32_t dst = sa + A_STAGE_BYTES + j * G::B_BOX_BYTES;
-                                if constexpr (MODE == 1) {
-                                    tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC, kc * G::KB);
-                                } else if (j % 2 == static_cast<int>(rank)) {
-                                    tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC,
-                                                          kc * G::KB, CLUSTER_MASK);
+                                for (int j = 0; j < BN / G::BOXC; ++j) {
+                                    const uint32_t dst = sc + A_STAGE_BYTES + j * G::B_BOX_BYTES;
+                                    if constexpr (MODE == 1) {
+                                        tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC, k0);
+                                    } else if (j % 2 == static_cast<int>(rank)) {
+                                        tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC, k0,
+                                                              CLUSTER_MASK);
+                                    }
                                 }
                             }
                         }
                         issued |= 1u << slot;
                         last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
                     }
-                    if (++slot == static_cast<uint32_t>(stages)) {
+                    slot += grp;
+                    if (slot == static_cast<uint32_t>(stages)) {
                         slot = 0;
                         phase ^= 1u;
                     }
@@ -784,44 +802,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * BN;
-                for (int kc = 0; kc < p.k_chunks; ++kc) {
+                // Slots come in groups of ring_group on one full and one empty
+                // barrier: each wait stalls this warp long enough for the tensor
+                // pipe to run dry, so fewer waits per MMA keep it busier.
+                for (int kc = 0; kc < p.k_chunks; kc += ring_group) {
                     if (!wait_all(full_bar(slot), phase, SITE_MMA_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = ring0 + slot * stage_bytes;
-                    // A: K-major, 8-row groups 1024 B apart.  B: MN-major, 8-K-row
-                    // groups 1024 B apart, 64-column blocks one TMA box apart.
-                    const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
-                    const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE_BYTES, G::B_BOX_BYTES, 1024);
-                    // K steps that lie wholly past K would only add products of
-                    // zero-filled elements: skip them
-                    const int ksteps = min(G::KB / G::UK, (p.K - kc * G::KB + G::UK - 1) / G::UK);
                     if (issuer) {
+                        const int nq = min(ring_group, p.k_chunks - kc);
+                        for (int c = 0; c < nq; ++c) {
+                            const int kk = kc + c;
+                            const uint32_t sa = ring0 + (slot + c) * stage_bytes;
+                            // A: K-major, 8-row groups 1024 B apart.  B: MN-major, 8-K-row
+                            // groups 1024 B apart, 64-column blocks one TMA box apart.
+                            const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
+                            const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE_BYTES, G::B_BOX_BYTES, 1024);
+                            // K steps that lie wholly past K would only add products of
+                            // zero-filled elements: skip them
+                            const int ksteps = min(G::KB / G::UK, (p.K - kk * G::KB + G::UK - 1) / G::UK);
 #pragma unroll
-                        for (int k = 0; k < G::KB / G::UK; ++k) {
-                            // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
-                            if (k < ksteps) {
-                                const uint64_t ad = a_desc + ((k * 32) >> 4);  // +32 bytes of K along the row
-                                const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
-                                const uint32_t acc = (kc | k) != 0 ? 1u : 0u;
-                                if constexpr (PAIR) {
-                                    umma_pair<ESZ>(d_tmem, ad, bd, p.idesc, acc);
-                                } else {
-                                    umma<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                            for (int k = 0; k < G::KB / G::UK; ++k) {
+                                // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
+                                if (k < ksteps) {
+                                    const uint64_t ad = a_desc + ((k * 32) >> 4);  // +32 bytes of K along the row
+                                    const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
+                                    const uint32_t acc = (kk | k) != 0 ? 1u : 0u;
+                                    if constexpr (PAIR) {
+                                        umma_pair<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                                    } else {
+                                        umma<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                                    }
                                 }
                             }
                         }
                         if constexpr (MODE == 1 || MODE == 4) {
                             umma_commit(empty_bar(slot));
                         } else if constexpr (MODE == 2) {
-                            umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slot in both CTAs
+                            umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slots in both CTAs
                         } else {
                             umma_commit_pair_multicast(empty_bar(slot), CLUSTER_MASK);
                         }
                     }
-                    if (++slot == static_cast<uint32_t>(stages)) {
+                    slot += ring_group;
+                    if (slot == static_cast<uint32_t>(stages)) {
                         slot = 0;
                         phase ^= 1u;
                     }

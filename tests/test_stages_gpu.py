@@ -178,3 +178,52 @@ def test_cluster_modes_bit_identical(bn):
         lib.sg_test_set_tile_n(0)
     for (m, mode, st), o in outs.items():
         assert np.array_equal(o, outs[(m, 1, 1)]), (m, mode, st)
+
+
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_paired_slots_odd_chunk_count(mode):
+    """With 6 or 8 ring slots and both operands copied by TMA, slots are
+    filled and consumed in pairs on one pair of barriers.  An odd number of
+    K chunks leaves each tile's last pair half used, and the next tile's
+    chunks start on the following pair; C must keep the single-slot bits
+    (the same MMAs in the same K order) in every kernel mode."""
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = sg.load_library()
+    M, N, K = 1300, 1100, 9 * 64 - 3                 # 9 K chunks, the last one ragged
+    a, b = seeded_case(M, N, K, "f16", seed=27 + mode, lda=576)
+    try:
+        assert lib.sg_test_set_cluster(mode) == 0
+        assert lib.sg_test_set_tile_n(128) == 0
+        p = _plan(M, N, K, "f16", "f32")
+        assert p["mode"] == mode and p["max_stages"] >= 6
+        grouped = {s: _plan(M, N, K, "f16", "f32", stages=s)["ring_group"] for s in range(1, p["max_stages"] + 1)}
+        assert grouped[6] == 2 and grouped[5] == 1 and grouped[4] == 1 and grouped[1] == 1
+        outs = {s: run_gpu(a, b, M, N, K, "f16", "f32", stages=s) for s in (1, 5, 6)}
+    finally:
+        lib.sg_test_set_cluster(0)
+        lib.sg_test_set_tile_n(0)
+    assert np.array_equal(outs[6], outs[1]) and np.array_equal(outs[5], outs[1])
+    rng = np.random.default_rng(mode)
+    rows = np.concatenate([rng.integers(0, M, 2000), np.full(N, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, 2000), np.arange(N)])
+    ref, _, S = oracle.gemm_at(a, b, rows, cols, "f16", "f32", K=K)
+    compare(outs[6][rows, cols], ref, S, "f32", f"paired slots, mode {mode}")
+
+
+def test_paired_slots_only_with_tma_operands():
+    """Element-load staging (an A pitch that TMA cannot take) and the
+    resident-B mode keep one barrier pair per slot."""
+    import tensor_core_gemm_tma_gb300 as sg
+    assert _plan(8192, 8192, 8192, "bf16", "bf16")["ring_group"] == 2
+    assert _plan(40000, 384, 96, "f16", "f16")["ring_group"] == 1      # mode 4
+    lib = sg.load_library()
+    M, N, K = 600, 500, 1000
+    a, b = seeded_case(M, N, K, "f16", seed=31, lda=1001)               # 2002-byte rows: element loads
+    try:
+        assert lib.sg_test_set_tile_n(128) == 0                           # a 6-slot ring
+        assert _plan(M, N, K, "f16", "f32")["max_stages"] >= 6
+        out = run_gpu(a, b, M, N, K, "f16", "f32")
+    finally:
+        lib.sg_test_set_tile_n(0)
+    ref, _, S = oracle.gemm(a, b, "f16", "f32", K=K)
+    compare(out, ref, S, "f32", "element loads, 6 slots")
