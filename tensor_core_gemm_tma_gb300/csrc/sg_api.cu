@@ -291,8 +291,10 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // counted as whole waves of tiles over the SMs times the time of one tile
     // (its width over its throughput relative to 256 columns).  Narrower tiles
     // stage more operand bytes per product, and with every SM loading that
-    // costs throughput: 192 columns ran at ~0.78 and 128 at ~0.55 of 256 on
-    // GB300.  Those ratios are rough, so a narrower width must win by 5%.  A
+    // costs throughput: on GB300 (8192^3, 8192^2 x 2048, 4096^3) 192 columns
+    // (single CTAs, a 4-slot ring) ran at ~0.64 of 256 and 128 (CTA pairs,
+    // 8 slots) at ~0.65.  Those ratios are rough, so a narrower width must
+    // win by 5%.  A
     // short K loop (<= 4 chunks) makes the epilogue the bottleneck: keep 128,
     // whose four tensor-memory accumulators overlap it best.
     int bn = 128;
@@ -300,7 +302,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
         double best = 0.0;
         for (int cand : {256, 192, 128}) {
             if (cand % boxc) continue;
-            const double rel = cand == 256 ? 1.0 : cand == 192 ? 0.78 : 0.55;
+            const double rel = cand == 256 ? 1.0 : cand == 192 ? 0.64 : 0.65;
             const int64_t waves = cdiv(pl->m_blocks * cdiv(N, cand), static_cast<int64_t>(st.sm_count));
             const double cost = static_cast<double>(waves) * cand / rel;
             if (best == 0.0 || cost < 0.95 * best) {
