@@ -26,12 +26,14 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 // Cluster row blocks swept together by the tile raster (L2 reuse of the B
-// tiles they share); STAGE_GEMM_GROUP_M overrides it at load (tuning only:
-// the order of tiles never changes a result).
+// tiles they share).  12 measured best on GB300 among 4-24 (8192^3 bf16 and
+// FP8, 4096^3, 16384 x 8192 x 4096, 6144 x 12288 x 4096): 0-4% over 8.
+// STAGE_GEMM_GROUP_M overrides it at load (tuning only: the order of tiles
+// never changes a result).
 const int kGroupM = [] {
     const char* e = std::getenv("STAGE_GEMM_GROUP_M");
     const int x = e ? std::atoi(e) : 0;
-    return (x >= 1 && x <= 64) ? x : 8;
+    return (x >= 1 && x <= 64) ? x : 12;
 }();
 
 struct DevState {
@@ -219,7 +221,7 @@ TuneKey tune_key(int dev, int64_t M, int64_t N, int64_t K, int in_dtype, int out
 struct Plan {
     int bn = 128;
     int block_k = 64;  // K elements per stage (128 bytes of K)
-    int group_m = 8;
+    int group_m = 12;
     int mode = 1;  // 1: single CTA, 2: CTA pairs sharing B by multicast, 3: paired MMA
     int cm = 1;    // CTAs per cluster along M
     int stages = 0, max_stages = 0;
@@ -774,13 +776,13 @@ int sg_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
         if (bn > 128 && N <= bn - 64) continue;  // a tile mostly past N
         for (int mode : {1, 2, 3}) {
             if (mode > 1 && ((bn / (128 / esz)) % 2 != 0 || m_blocks < 2 || !a_tma || !b_tma)) continue;
-            for (int g : {4, 8, 16}) {
+            for (int g : {4, 8, 12, 16}) {
                 Choice c;
                 c.bn = bn;
                 c.mode = mode;
                 c.group_m = g;
                 // the raster only matters when there are more tiles than CTAs
-                if (g != 8 && m_blocks * cdiv(N, bn) <= st->sm_count) continue;
+                if (g != 12 && m_blocks * cdiv(N, bn) <= st->sm_count) continue;
                 cands.push_back(c);
             }
         }
