@@ -94,7 +94,7 @@ enum {
 };
 
 #define SG_MAX_STAGES 8
-#define SG_VERSION 100 /* 1.0.0 */
+#define SG_VERSION 110 /* 1.1.0: sg_plan_info gained tail_units */
 
 /*
  * sg_gemm -- C[i*ldc + j] = epilogue(sum_k A[i*lda + k] * B[k*ldb + j])
@@ -239,6 +239,11 @@ typedef struct {
     int32_t ring_group;    /* ring slots filled and consumed together on one
                               pair of barriers (2 when both operands arrive by
                               TMA and the ring has 6 or 8 slots, else 1) */
+    int32_t tail_units;    /* half-width units the last tiles of the raster
+                              were split into (0: none): when a last wave of
+                              256-column tiles (16-bit operands, both by TMA)
+                              would fill at most half of the clusters, each of
+                              its tiles runs as two 128-column units */
 } sg_plan_info;
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,

@@ -52,6 +52,15 @@ int sg_test_set_tile_n(int bn);
  */
 int sg_test_set_cluster(int mode);
 
+/*
+ * Whether later plans may split a short last wave of 256-column tiles into
+ * 128-column units (1, the default) or never (0).  Every element is computed
+ * by one unit either way, summing the same products in the same K order, so
+ * C must be bit-identical.  Returns 0, or SG_ERR_ARG.  The environment
+ * variable STAGE_GEMM_TAIL_SPLIT=0 sets the initial value at load.
+ */
+int sg_test_set_tail_split(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -44,7 +44,7 @@ class SgError(RuntimeError):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "block_n", "block_k", "stages", "max_stages", "tiles", "grid", "threads", "smem_bytes",
-        "tmem_columns", "tma_store", "cluster_m", "pair_mma", "group_m", "mode", "ring_group")]
+        "tmem_columns", "tma_store", "cluster_m", "pair_mma", "group_m", "mode", "ring_group", "tail_units")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -101,6 +101,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.sg_test_set_tile_n.argtypes = [i32]
         lib.sg_test_set_cluster.restype = i32
         lib.sg_test_set_cluster.argtypes = [i32]
+        lib.sg_test_set_tail_split.restype = i32
+        lib.sg_test_set_tail_split.argtypes = [i32]
         if path is None:
             _lib = lib
         return lib

@@ -226,6 +226,7 @@ struct Plan {
     int cm = 1;    // CTAs per cluster along M
     int stages = 0, max_stages = 0;
     int ring_group = 1;  // ring slots sharing one full and one empty barrier
+    int64_t units = 0, full_units = 0;  // work units launched; those of whole tiles (the rest: half tiles)
     int64_t m_blocks = 0, n_blocks = 0, tiles = 0, k_chunks = 0;
     int grid = 0;
     int smem = 0;
@@ -269,6 +270,14 @@ std::atomic<int> g_force_bn{[] {
     return e ? valid_bn(std::atoi(e)) : 0;
 }()};
 int forced_bn() { return g_force_bn.load(); }
+
+// Splitting a short last wave of 256-column tiles into half tiles, set by
+// sg_test_set_tail_split or, at load, the environment variable
+// STAGE_GEMM_TAIL_SPLIT (0: never; 1: where it pays, the default).
+std::atomic<int> g_tail_split{[] {
+    const char* e = std::getenv("STAGE_GEMM_TAIL_SPLIT");
+    return (e && std::atoi(e) == 0) ? 0 : 1;
+}()};
 
 // Kernel mode forced by sg_test_set_cluster or, at load, the environment
 // variable STAGE_GEMM_CLUSTER (1: single CTA, 2: CTA pairs sharing B by
@@ -383,7 +392,20 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // SM's shared memory.
     if (pl->tmem_cols > 256 && pl->smem <= st.smem_per_sm / 2) pl->smem = st.smem_per_sm / 2 + 1024;
     const int64_t clusters = st.sm_count / cm;
-    pl->grid = static_cast<int>((pl->tiles < clusters ? pl->tiles : clusters) * cm);
+    // A last wave that fills at most half of the clusters takes as long as a
+    // full one.  Its tiles, when 256 columns wide (16-bit operands, both by
+    // TMA), are split into two 128-column units each, so that wave spreads
+    // over twice as many clusters and takes about half as long (the other
+    // waves are unchanged).  Each output element is still computed by one
+    // unit, summing the same products in the same K order: C keeps its bits.
+    pl->units = pl->full_units = pl->tiles;
+    const int64_t tail = pl->tiles % clusters;
+    if (g_tail_split.load() && !panel && esz == 2 && bn == 256 && a_tma && b_tma && pl->k_chunks > 0 &&
+        pl->tiles > clusters && tail > 0 && 2 * tail <= clusters) {
+        pl->full_units = pl->tiles - tail;
+        pl->units = pl->full_units + 2 * tail;
+    }
+    pl->grid = static_cast<int>((pl->units < clusters ? pl->units : clusters) * cm);
     const int oes = elem_bytes(out_dtype);
     pl->tma_store = ((reinterpret_cast<uintptr_t>(C) & 15) == 0 && (M == 1 || (ldc * oes) % 16 == 0)) ? 1 : 0;
     return SG_OK;
@@ -467,6 +489,7 @@ void fill_info(const Plan& pl, sg_plan_info* info) {
     info->group_m = pl.group_m;
     info->mode = pl.mode;
     info->ring_group = pl.ring_group;
+    info->tail_units = static_cast<int32_t>(pl.units - pl.full_units);
 }
 
 bool c_tma_legal(const void* C, int64_t M, int64_t ldc, int out_dtype) {
@@ -537,7 +560,8 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.K = static_cast<int32_t>(K);
     prm.m_blocks = static_cast<int32_t>(pl.m_blocks);
     prm.n_blocks = static_cast<int32_t>(pl.n_blocks);
-    prm.num_tiles = static_cast<int32_t>(pl.tiles);
+    prm.num_tiles = static_cast<int32_t>(pl.units);
+    prm.full_units = static_cast<int32_t>(pl.full_units);
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
     prm.ring_group = pl.ring_group;
@@ -545,6 +569,8 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     const int mma_m = pl.mode == 3 ? 2 * sg::BM : sg::BM;
     prm.idesc = esz == 1 ? sg::idesc_e4m3(mma_m, pl.bn, true)
                          : sg::idesc_f16(in_dtype == SG_BF16, mma_m, pl.bn, true);
+    prm.idesc_half = esz == 1 ? sg::idesc_e4m3(mma_m, pl.bn / 2, true)
+                              : sg::idesc_f16(in_dtype == SG_BF16, mma_m, pl.bn / 2, true);
     prm.epi = epilogue;
     prm.tma_store = pl.tma_store;
     prm.bias = bias;
@@ -902,6 +928,12 @@ int sg_test_set_tile_n(int bn) {
 int sg_test_set_cluster(int mode) {
     if (mode < 0 || mode > 4) return SG_ERR_ARG;
     g_force_mode.store(mode);
+    return SG_OK;
+}
+
+int sg_test_set_tail_split(int on) {
+    if (on != 0 && on != 1) return SG_ERR_ARG;
+    g_tail_split.store(on);
     return SG_OK;
 }
 

@@ -137,7 +137,14 @@ struct Layout {
 
 struct Params {
     int32_t M, N, K;
-    int32_t m_blocks, n_blocks, num_tiles, k_chunks;  // num_tiles counts cluster tiles (CM row blocks each)
+    int32_t m_blocks, n_blocks, num_tiles, k_chunks;  // num_tiles counts work units (below)
+    // Work units: units below full_units are whole cluster tiles (CM row
+    // blocks by BN columns) in raster order; the tiles after them, the last
+    // ones of the raster, are each split into two units of BN / 2 columns
+    // (their left half first) so that a short last wave spreads over twice
+    // as many clusters.  Without a split full_units == num_tiles.
+    int32_t full_units;
+    uint32_t idesc_half;   // tcgen05 instruction descriptor of a half-width unit
     int32_t stages;
     int32_t ring_group;    // ring slots filled and consumed together on one barrier pair (1 or 2)
     int32_t group_m;       // tile raster: group_m row-blocks swept together for L2 reuse
@@ -256,6 +263,23 @@ __device__ __forceinline__ void tile_coords(int tile, const Params& p, uint32_t 
     const int r = tile - g * per_group;
     mb = (first_m + r % gsize) * CM + static_cast<int>(rank);
     nb = r / gsize;
+}
+
+// Row block and first column of work unit `u` (modes 1-3); returns its width
+// in columns.  Only 256-column tiles of 16-bit operands are ever split: each
+// half is then a whole number of 64-column B boxes in every CTA.
+template <int CM, int BN, int ESZ>
+__device__ __forceinline__ int unit_coords(int u, const Params& p, uint32_t rank, int& mb, int& col0) {
+    int nb;
+    if (BN != 256 || ESZ != 2 || u < p.full_units) {
+        tile_coords<CM>(u, p, rank, mb, nb);
+        col0 = nb * BN;
+        return BN;
+    }
+    const int v = u - p.full_units;
+    tile_coords<CM>(p.full_units + (v >> 1), p, rank, mb, nb);
+    col0 = nb * BN + (v & 1) * (BN / 2);
+    return BN / 2;
 }
 
 // Wait for phase `parity` of `bar`, giving up after `limit` ns or when another
@@ -669,8 +693,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         bres_bar, nb * BN + j * G::BOXC, kc * G::KB);
             }
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
-                int mb = tile, nb = 0;
-                if constexpr (!PANEL) tile_coords<CM>(tile, p, rank, mb, nb);
+                int mb = tile, col0 = 0, width = BN;
+                if constexpr (!PANEL) width = unit_coords<CM, BN, ESZ>(tile, p, rank, mb, col0);
+                // B columns landing in this CTA per K chunk: the paired MMA stages
+                // half of the unit's columns in each CTA; mode 2 multicasts every
+                // box into both CTAs
+                const int bl = PAIR ? width / 2 : width;
+                const uint32_t chunk_tx = A_STAGE_BYTES + static_cast<uint32_t>(bl) * BK_BYTES;
                 const int fills = PANEL ? 1 : p.k_chunks;  // mode 4: one ring slot holds every K chunk of A
                 const int grp = PANEL ? 1 : ring_group;
                 for (int kc = 0; kc < fills; kc += grp, it += grp) {
@@ -689,29 +718,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         } else if constexpr (PAIR) {
                             // both CTAs' copies complete on the even CTA's barrier
                             const uint32_t fb = mapa_shared(full_bar(slot), 0);
-                            if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), nq * 2 * L::STAGE_BYTES);
+                            if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), nq * 2 * chunk_tx);
                             for (int c = 0; c < nq; ++c) {
                                 const uint32_t sc = sa + c * stage_bytes;
                                 const int k0 = (kc + c) * G::KB;
                                 tma_load_2d_pair(sc, &tmA, fb, k0, mb * BM);
-#pragma unroll
-                                for (int j = 0; j < BL / G::BOXC; ++j)
+                                for (int j = 0; j < bl / G::BOXC; ++j)
                                     tma_load_2d_pair(sc + A_STAGE_BYTES + j * G::B_BOX_BYTES, &tmB, fb,
-                                                     nb * BN + static_cast<int>(rank) * BL + j * G::BOXC, k0);
+                                                     col0 + static_cast<int>(rank) * bl + j * G::BOXC, k0);
                             }
                         } else {
-                            mbar_arrive_expect_tx(full_bar(slot), nq * L::STAGE_BYTES);
+                            mbar_arrive_expect_tx(full_bar(slot), nq * chunk_tx);
                             for (int c = 0; c < nq; ++c) {
                                 const uint32_t sc = sa + c * stage_bytes;
                                 const int k0 = (kc + c) * G::KB;
                                 tma_load_2d(sc, &tmA, full_bar(slot), k0, mb * BM);
-#pragma unroll
-                                for (int j = 0; j < BN / G::BOXC; ++j) {
+                                for (int j = 0; j < width / G::BOXC; ++j) {
                                     const uint32_t dst = sc + A_STAGE_BYTES + j * G::B_BOX_BYTES;
                                     if constexpr (MODE == 1) {
-                                        tma_load_2d(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC, k0);
+                                        tma_load_2d(dst, &tmB, full_bar(slot), col0 + j * G::BOXC, k0);
                                     } else if (j % 2 == static_cast<int>(rank)) {
-                                        tma_load_2d_multicast(dst, &tmB, full_bar(slot), nb * BN + j * G::BOXC, k0,
+                                        tma_load_2d_multicast(dst, &tmB, full_bar(slot), col0 + j * G::BOXC, k0,
                                                               CLUSTER_MASK);
                                     }
                                 }
@@ -802,6 +829,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + ab * BN;
+                int umb, ucol;
+                const uint32_t idesc = unit_coords<CM, BN, ESZ>(tile, p, rank, umb, ucol) == BN ? p.idesc : p.idesc_half;
                 // Slots come in groups of ring_group on one full and one empty
                 // barrier: each wait stalls this warp long enough for the tensor
                 // pipe to run dry, so fewer waits per MMA keep it busier.
@@ -831,9 +860,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
                                     const uint32_t acc = (kk | k) != 0 ? 1u : 0u;
                                     if constexpr (PAIR) {
-                                        umma_pair<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                                        umma_pair<ESZ>(d_tmem, ad, bd, idesc, acc);
                                     } else {
-                                        umma<ESZ>(d_tmem, ad, bd, p.idesc, acc);
+                                        umma<ESZ>(d_tmem, ad, bd, idesc, acc);
                                     }
                                 }
                             }
@@ -916,12 +945,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // units: one per tile (modes 1-3), or (row tile, column block) pairs (modes 4, 5)
         const int subs = PANEL ? p.n_blocks : 1;
         for (int tile = cluster_id, sub = 0; tile < p.num_tiles;) {
-            int mb = tile, nb = sub;
-            if constexpr (!PANEL) tile_coords<CM>(tile, p, rank, mb, nb);
+            int mb = tile, ucol = sub * BN, width = BN;
+            if constexpr (!PANEL) width = unit_coords<CM, BN, ESZ>(tile, p, rank, mb, ucol);
             const int row0 = mb * BM + q * 32;
             const int row = row0 + lane;
             // the residual of this warp's first chunk loads while the MMAs run
-            if (r_staged && row0 < p.M && nb * BN + part * COLS < p.N) load_residual(row0, nb * BN + part * COLS);
+            if (r_staged && row0 < p.M && ucol + part * COLS < p.N) load_residual(row0, ucol + part * COLS);
             if (p.k_chunks > 0) {
                 const bool w = wait_bounded(tfull_bar(ab), aph, abort_flag, p.status, p.wait_limit_ns,
                                             SITE_EPI_TMEM_FULL);
@@ -930,8 +959,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN;
 #pragma unroll 1
-            for (int c = part * COLS; c < BN; c += SPLIT * COLS) {
-                const int col0 = nb * BN + c;
+            for (int c = part * COLS; c < width; c += SPLIT * COLS) {
+                const int col0 = ucol + c;
                 float v[COLS];
                 if (p.k_chunks > 0) {
                     uint32_t r[32];
@@ -1027,7 +1056,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();  // the next tcgen05.ld is warp-collective
                 // the next chunk's residual (the store just issued must read the buffer first)
                 const int cn = c + SPLIT * COLS;
-                if (r_staged && cn < BN && row0 < p.M && nb * BN + cn < p.N) load_residual(row0, nb * BN + cn);
+                if (r_staged && cn < width && row0 < p.M && ucol + cn < p.N) load_residual(row0, ucol + cn);
             }
             if (p.k_chunks > 0) {
                 tc_fence_before();

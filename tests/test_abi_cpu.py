@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(sg):
 
 
 def test_version_and_strerror(sg):
-    assert sg.version() == 100
+    assert sg.version() == 110
     for code in range(0, -9, -1):
         txt = sg.strerror(code)
         assert txt and txt != "unknown error code"
