@@ -12,8 +12,11 @@ tensor-core roofline case.  Other workloads: see gemm_inputs.WORKLOADS.
 
 Timing: W untimed warm-up steps; then K steps bracketed by a barrier and a
 device synchronisation; each step's GEMM is timed with CUDA events on the
-launching stream, and a 256 MiB buffer is written between steps (outside
-the events) so every step starts with a cold L2.  `value` is the whole-job
+launching stream, and L2 is flushed between steps (outside the events) so
+every step starts with a cold L2: by default a 256 MiB buffer is written and
+a second 256 MiB buffer then read, so the write's dirty lines are written
+back before the timed launch instead of during it (--flush write: the write
+alone).  `value` is the whole-job
 throughput: total FLOPs of all ranks / max-over-ranks of the summed event
 time.  With N > 1 every rank runs an independent replica (the path has no
 exchange step; "weak" scaling).
@@ -42,6 +45,13 @@ if ROOT not in sys.path:
 import gemm_inputs  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20
+NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s of HBM3e the skinny-K target is stated against
+# The only timing on the pages: a whole 4K denoiser frame (11 Swin layers,
+# not one GEMM), on hardware the page does not name.  Context, not a target.
+PAGES_CONTEXT = {"what": "whole 3840x2160 denoiser frame: isolated native phase-8 splice vs translated body",
+                 "ms": {"splice": 14.90, "translated": 6.59}, "hardware": "not named on the page",
+                 "source": "d4r, rrswin_enc2_epilogues.md (page header)",
+                 "note": "context only: a whole-frame time of another engine, not comparable to one GEMM"}
 METRIC = "GEMM TFLOP/s and % of GB300 dense fp16/bf16 peak (HBM GB/s for skinny-K)"
 DEFAULT_WORKLOAD = "square8192_bf16"
 HBM_BOUND = {"swin4k_proj_f16", "swin4k_backproj_f16", "swin4k_proj_i8w"}
@@ -62,6 +72,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--tune", action="store_true",
                     help="tune the launch configuration first (sg_tune) instead of the planner's heuristic")
+    ap.add_argument("--flush", default="write+read", choices=["write+read", "write"],
+                    help="L2 flush between timed steps: a 256 MiB write then a 256 MiB read (clean cold L2), "
+                         "or the write alone (its dirty lines are written back during the timed launch)")
+    ap.add_argument("--block-n", type=int, default=0, help="sg_config.block_n (0: the planner's)")
+    ap.add_argument("--mode", type=int, default=0, help="sg_config.mode (0: the planner's)")
     return ap.parse_args()
 
 
@@ -226,6 +241,59 @@ def oracle_rows(w, a, b, bias, r, rows, threads):
                        R_bits=None if r is None else r[:rows], r_dtype=w.out_dtype if r is not None else None)
 
 
+def cpu_baseline_entry(w, target_s):
+    """The oracle (as it stands) timed on the host cores on a row-block
+    sample of the workload, as a cpu_baseline object."""
+    dt, rows, flops, threads = cpu_oracle_sample(w, target_s=target_s)
+    d = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+         "sample": f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product ({rows * w.N} outputs, {dt:.2f} s)",
+         "extrapolated": rows < w.M, "seconds": dt}
+    if w.name in HBM_BOUND:
+        d["gbs"] = w.algorithmic_bytes * rows / w.M / dt / 1e9
+    return d
+
+
+def call_latency(sg, w, device, stream, calls=200):
+    """Per-call latency of a launch-bound product: the device time of back to
+    back launches (no flush), the host time per stage_gemm call (the ctypes
+    call and the launch, synchronised once at the end), and one
+    host-buffer call (stage_gemm_host: copies in, GEMM, copy out) end to end."""
+    import torch
+    A_h, B_h, bias_h, R_h = device_inputs(w, device)
+    A, B = A_h.to(device), B_h.to(device)
+    C = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            sg.stage_gemm(A, B, epilogue=w.epilogue, out=C, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(calls):
+            sg.stage_gemm(A, B, epilogue=w.epilogue, out=C, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        host_us = (time.perf_counter() - t0) / calls * 1e6
+        dev_us = e0.elapsed_time(e1) / calls * 1e3
+        A_p, B_p = A_h.pin_memory(), B_h.pin_memory()
+        out_h = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), pin_memory=True)
+        for _ in range(5):
+            sg.stage_gemm_host(A_p, B_p, out_dtype=out_h.dtype, epilogue=w.epilogue, device=device, stream=stream,
+                               out_host=out_h)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(50):
+            t0 = time.perf_counter()
+            sg.stage_gemm_host(A_p, B_p, out_dtype=out_h.dtype, epilogue=w.epilogue, device=device, stream=stream,
+                               out_host=out_h)
+            stream.synchronize()
+            ts.append((time.perf_counter() - t0) * 1e6)
+    return {"device_us_per_launch_back_to_back": dev_us, "host_us_per_call_back_to_back": host_us,
+            "host_buffer_call_us_median": statistics.median(ts),
+            "how": f"{calls} back-to-back stage_gemm calls on resident operands (CUDA events; host wall clock); "
+                   "50 synchronised stage_gemm_host calls on pinned buffers (copies in and out included)"}
+
+
 def cpu_oracle_sample(w, target_s=12.0, a=None, b=None, bias=None):
     """Time the oracle (as it stands) on a row-block sample of the workload:
     returns (seconds, rows, flops, threads)."""
@@ -274,17 +342,18 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, plan):
+def config_of(w, plan, flush_mode="write+read"):
+    how = {"write+read": "a 256 MiB write then a 256 MiB read", "write": "a 256 MiB write"}[flush_mode]
     c = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "in_dtype": w.in_dtype, "out_dtype": w.out_dtype,
          "epilogue": w.epilogue, "accumulate": "f32", "layout": "A, B, C row-major, dense",
-         "l2": "flushed between timed steps (256 MiB write outside the timed events)",
+         "l2": f"flushed between timed steps ({how}, outside the timed events)",
          "description": w.description}
     if plan:
         rows = plan["block_m"] * (2 if plan.get("pair_mma") else 1)
         c["tile"] = f"{rows}x{plan['block_n']}x{plan['block_k']}"
         c["stages"] = plan["stages"]
         c["grid"] = plan["grid"]
-        c["kernel_mode"] = {1: "single CTA", 2: "CTA pair, B multicast", 3: "paired MMA (cta_group::2)",
+        c["kernel_mode"] = {1: "single CTA", 3: "paired MMA (cta_group::2)",
                             4: "resident B (one CTA per row tile, all of B in shared memory)",
                             5: "decoded panel (int8-coded B decoded once per CTA into the resident shared-memory "
                                "panel)"}.get(plan.get("mode"))
@@ -293,7 +362,22 @@ def config_of(w, plan):
     return c
 
 
-def measure(sg, w, device, stream, steps, warmup, stages, inputs=None, tune=True):
+def make_flush(device, mode):
+    """The L2 flush run between timed steps (outside the events)."""
+    import torch
+    wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    if mode == "write":
+        return lambda: wbuf.fill_(1)
+    rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        wbuf.fill_(1)
+        rbuf.sum()          # reads 256 MiB: the write's dirty lines leave L2 here
+    return flush
+
+
+def measure(sg, w, device, stream, steps, warmup, stages, inputs=None, tune=True, config=None,
+            flush_mode="write+read"):
     import torch
     A_h, B_h, bias_h, R_h = inputs if inputs is not None else device_inputs(w, device)
     A = A_h.to(device)
@@ -301,19 +385,17 @@ def measure(sg, w, device, stream, steps, warmup, stages, inputs=None, tune=True
     bias = None if bias_h is None else bias_h.to(device)
     R = None if R_h is None else R_h.to(device)
     C = torch.empty((w.M, w.N), dtype=out_torch_dtype(w), device=device)
-    if tune and stages == 0 and R is None and not w.b_coded:
+    if tune and config is None and stages == 0 and R is None and not w.b_coded:
         # the library's own tuner picks the configuration (outside the timed steps)
         sg.tune(A, B, epilogue=w.epilogue, bias=bias, out=C, stream=stream)
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = make_flush(device, flush_mode)
 
     def call():
         if w.b_coded:
             sg.stage_gemm_qb(A, B[0], B[1], epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream)
         else:
-            sg.stage_gemm(A, B, epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream, residual=R)
-
-    def flush():
-        flush_buf.fill_(1)
+            sg.stage_gemm(A, B, epilogue=w.epilogue, bias=bias, stages=stages, out=C, stream=stream, residual=R,
+                          config=config)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -378,7 +460,7 @@ def whole_job_tflops(flops_per_step: float, world: int, steps: int, max_sum_ms: 
     return flops_per_step * world * steps / (max_sum_ms * 1e-3) / 1e12
 
 
-def dram_reference(device, nbytes_write: int, steps: int = 10):
+def dram_reference(device, nbytes_write: int, steps: int = 10, flush_mode="write+read"):
     """Same-run DRAM references for an HBM-bound workload: a device memset
     of the workload's output bytes (write only) and a device-to-device copy
     of as many bytes (read + write), each timed like the GEMM (L2 flushed
@@ -387,14 +469,14 @@ def dram_reference(device, nbytes_write: int, steps: int = 10):
     n = (nbytes_write + 1) // 2
     x = torch.empty(n, dtype=torch.float16, device=device)
     y = torch.empty(n, dtype=torch.float16, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = make_flush(device, flush_mode)
 
     def med(fn):
         for _ in range(2):
             fn()
         ts = []
         for _ in range(steps):
-            flush.fill_(1)
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -408,7 +490,7 @@ def dram_reference(device, nbytes_write: int, steps: int = 10):
             "bytes": 2 * n, "how": "cudaMemsetAsync of the output's bytes; device copy of as many bytes (read+write)"}
 
 
-def library_reference(w, dev_tensors, stream, steps=10, warmup=3):
+def library_reference(w, dev_tensors, stream, steps=10, warmup=3, flush_mode="write+read"):
     """Same-run library reference for a tensor-bound fp16/bf16 workload: the
     same product through torch.matmul (cuBLAS) plus torch's own ReLU / bias
     ops for the epilogue, on the same device tensors, timed like the GEMM (L2
@@ -418,7 +500,7 @@ def library_reference(w, dev_tensors, stream, steps=10, warmup=3):
     if w.name in HBM_BOUND or w.dist_r is not None or w.b_coded:
         return None
     A, B, bias, C = dev_tensors
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=A.device)
+    flush = make_flush(A.device, flush_mode)
     if w.in_dtype == "e4m3":
         # cuBLAS FP8 through torch._scaled_mm: unit scales, fp32 accumulation
         # (use_fast_accum=False), B column-major as it requires (laid out
@@ -441,9 +523,6 @@ def library_reference(w, dev_tensors, stream, steps=10, warmup=3):
                 C.relu_()
         impl = "torch.matmul (cuBLAS)" + (" + torch ReLU" if w.epilogue != "none" else "")
 
-    def flush():
-        flush_buf.fill_(1)
-
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             flush()
@@ -454,12 +533,18 @@ def library_reference(w, dev_tensors, stream, steps=10, warmup=3):
     return {"impl": impl, "value": w.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms}
 
 
-def roofline_of(w, ms, peaks, traffic):
+def roofline_of(w, ms, peaks, traffic, library=None):
+    """The dominant (only) kernel's roofline.  `frac` is against the measured
+    peak; for a tensor-bound workload with a same-run library figure,
+    `frac_conservative` is against the larger of the two (a library kernel
+    that beats the measured peak makes that the honest denominator); an
+    HBM-bound one also gets its fraction of the nominal ~8 TB/s."""
     if w.name in HBM_BOUND:
         achieved = w.algorithmic_bytes / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                 "algorithmic_bytes_per_launch": w.algorithmic_bytes}
     achieved = w.flops / (ms * 1e-3) / 1e12
     # fp16 and bf16 dense tensor rates are the same (nominal ratio 1); FP8 is
@@ -469,9 +554,15 @@ def roofline_of(w, ms, peaks, traffic):
     src = f"{peaks['source']} bf16_tflops (burst; kernel timed alone)"
     if ratio != 1.0:
         src += " x 2 (nominal FP8 : bf16 dense ratio)"
-    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": traffic, "peak_source": src,
-            "algorithmic_flops_per_launch": w.flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
+    r = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+         "frac": achieved / peak, "traffic": traffic, "peak_source": src,
+         "algorithmic_flops_per_launch": w.flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
+    if library is not None:
+        denom = max(peak, library["value"])
+        r["frac_conservative"] = achieved / denom
+        r["frac_conservative_of"] = ("same-run library " + library["impl"]) if library["value"] > peak else \
+            "measured peak (above the same-run library)"
+    return r
 
 
 def main():
@@ -506,23 +597,28 @@ def main():
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     clocks = ClockSampler(cvd.split(",")[local] if cvd else local)
     host_inputs = device_inputs(w, device)
+    cfg = None
+    if args.block_n or args.mode:
+        cfg = {"block_n": args.block_n, "mode": args.mode}
     # warm-up + timed steps (the clock sampler runs over the timed region)
     with clocks:
         barrier()
         times, host_inputs, dev_tensors = measure(sg, w, device, stream, args.steps, args.warmup, args.stages,
-                                                  inputs=host_inputs, tune=args.tune)
+                                                  inputs=host_inputs, tune=args.tune, config=cfg,
+                                                  flush_mode=args.flush)
         barrier()
     sum_ms = max_over_ranks(sum(times), pg, device)
     ms = sum_ms / len(times)
     value = whole_job_tflops(w.flops, world, len(times), sum_ms)
-    plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages)
+    plan = sg.plan(w.M, w.N, w.K, host_inputs[0].dtype, out_torch_dtype(w), w.epilogue, args.stages,
+                   config=None if w.b_coded else cfg)
     if w.b_coded:
         plan["mode"] = 5  # mode 4's geometry with the panel decoded from int8 codes (stage_gemm_qb)
-    plan["tuned"] = args.tune and args.stages == 0 and w.dist_r is None
+    plan["tuned"] = args.tune and cfg is None and args.stages == 0 and w.dist_r is None
 
     lib_ref = None
     if rank == 0 and not args.no_library_reference:
-        lib_ref = library_reference(w, dev_tensors, stream)
+        lib_ref = library_reference(w, dev_tensors, stream, flush_mode=args.flush)
         if lib_ref is not None:
             lib_ref["ours_over_library"] = (w.flops / (ms * 1e-3) / 1e12) / lib_ref["value"]
 
@@ -538,66 +634,88 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic (seeded SplitMix64, see gemm_inputs)",
-        "config": config_of(w, plan),
-        "roofline": roofline_of(w, ms, peaks, recorded_traffic(w.name)),
+        "config": config_of(w, plan, args.flush),
+        "roofline": roofline_of(w, ms, peaks, recorded_traffic(w.name), lib_ref),
         "ms_per_step_min": min(times), "ms_per_step_median": statistics.median(times),
         "gpu_launches": len(times),
-        "gpu_launches_note": "one stage_gemm kernel launch per timed step (the L2 flush between steps is a torch fill)",
+        "gpu_launches_note": "one stage_gemm kernel launch per timed step (the L2 flush between steps is torch "
+                             "fill and sum kernels, outside the timed events)",
         "clocks": clocks.summary(),
         "e2e": e2e,
         "kernel_source_hash": kernel_source_hash(),
+        "pages_context": PAGES_CONTEXT,
     }
     if lib_ref is not None:
         line["library_reference"] = lib_ref
     if w.name in HBM_BOUND:
         line["hbm_gbs"] = line["roofline"]["achieved"]
         out_bytes = w.M * w.N * {"f32": 4, "f16": 2, "bf16": 2}[w.out_dtype]
-        line["dram_reference"] = dram_reference(device, out_bytes)
+        line["dram_reference"] = dram_reference(device, out_bytes, flush_mode=args.flush)
 
-    if rank == 0 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD:
-        sec = []
-        for name in ("relu4096_f16", "swin4k_proj_f16", "swin4k_backproj_f16", "square8192_e4m3", "swin4k_proj_i8w"):
-            ws = gemm_inputs.WORKLOADS[name]
-            t2, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=args.tune)
-            m2 = sum(t2) / len(t2)
-            entry = {"workload": name, "ms_per_step": m2, "TFLOP/s": ws.flops / (m2 * 1e-3) / 1e12,
-                     "roofline": roofline_of(ws, m2, peaks, recorded_traffic(name))}
-            lr = None if args.no_library_reference else library_reference(ws, dt, stream)
-            if lr is not None:
-                lr["ours_over_library"] = entry["TFLOP/s"] / lr["value"]
-                entry["library_reference"] = lr
-            del dt
-            sec.append(entry)
-            if name == "relu4096_f16":
-                # the same product with the pages' tiling (a workgroup per 128 x 128
-                # output tile, gizml:tile's fused example): forced through the
-                # testing hooks; every tiling computes the same bits
-                lib = sg.load_library()
-                lib.sg_test_set_tile_n(128)
-                lib.sg_test_set_cluster(1)
-                try:
-                    t3, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=False)
-                    p3 = sg.plan(ws.M, ws.N, ws.K, torch.float16, torch.float16, ws.epilogue)
-                finally:
-                    lib.sg_test_set_tile_n(0)
-                    lib.sg_test_set_cluster(0)
-                del dt
-                m3 = sum(t3) / len(t3)
-                sec.append({"workload": name, "tiling": f"{p3['block_m']}x{p3['block_n']} single-CTA tiles "
-                                                        "(the pages' 128 x 128 output tile)",
-                            "ms_per_step": m3, "TFLOP/s": ws.flops / (m3 * 1e-3) / 1e12,
-                            "roofline": roofline_of(ws, m3, peaks, None)})
-        line["secondary"] = sec
+    if rank == 0 and not args.no_secondary and args.workload == DEFAULT_WORKLOAD and cfg is None:
+        line["secondary"] = secondaries(sg, device, stream, peaks, args)
 
     if rank == 0 and not args.no_cpu_baseline and world >= 1:
-        dt, rows, flops, threads = cpu_oracle_sample(w)
-        line["cpu_baseline"] = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product "
-                                          f"({rows * w.N} outputs, {dt:.1f} s)"}
+        line["cpu_baseline"] = cpu_baseline_entry(w, 12.0)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+# The other workloads, each measured as the main one is (10 timed steps after
+# 3 warm-up steps, L2 flushed between steps), with its own roofline, same-run
+# library figure where there is one, and its own CPU-oracle baseline.  The
+# 4096^3 ReLU product also runs in the pages' tiling (128 x 128 output tiles:
+# one CTA per tile, and CTA pairs whose CTAs each own one 128 x 128 tile).
+SECONDARY = ["square256_f16", "ragged1000_f16", "relu4096_f16", "swin4k_proj_f16", "swin4k_backproj_f16",
+             "square8192_e4m3", "swin4k_proj_i8w"]
+PAGES_TILINGS = [({"block_n": 128, "mode": 3}, "128x128 output tile per CTA, CTA pairs sharing B (paired MMA)"),
+                 ({"block_n": 128, "mode": 1}, "128x128 output tile per CTA, one CTA per tile")]
+
+
+def secondaries(sg, device, stream, peaks, args):
+    out = []
+
+    def one(ws, config=None, label=None):
+        t, _, dt = measure(sg, ws, device, stream, 10, 3, 0, tune=args.tune, config=config, flush_mode=args.flush)
+        m = sum(t) / len(t)
+        lr = None if args.no_library_reference or config is not None else \
+            library_reference(ws, dt, stream, flush_mode=args.flush)
+        del dt
+        p = sg.plan(ws.M, ws.N, ws.K, out_dt_in(ws), out_torch_dtype(ws), ws.epilogue, config=config) \
+            if not ws.b_coded else None
+        e = {"workload": ws.name, "ms_per_step": m, "TFLOP/s": ws.flops / (m * 1e-3) / 1e12,
+             "roofline": roofline_of(ws, m, peaks, recorded_traffic(ws.name) if config is None else None, lr)}
+        if p is not None:
+            e["plan"] = {k: p[k] for k in ("block_m", "block_n", "mode", "pair_mma", "stages", "grid", "tiles")}
+        if label:
+            e["tiling"] = label
+            e["config"] = config
+        if lr is not None:
+            lr["ours_over_library"] = e["TFLOP/s"] / lr["value"]
+            e["library_reference"] = lr
+        return e
+
+    for name in SECONDARY:
+        ws = gemm_inputs.WORKLOADS[name]
+        e = one(ws)
+        if name == "square256_f16":
+            e["latency"] = call_latency(sg, ws, device, stream)
+        if name in ("swin4k_proj_f16", "swin4k_proj_i8w"):
+            e["pages_context"] = "see the line's pages_context (a whole-frame figure, not this GEMM)"
+        if not args.no_cpu_baseline:
+            e["cpu_baseline"] = cpu_baseline_entry(ws, 2.5)
+        out.append(e)
+        if name == "relu4096_f16":
+            for config, label in PAGES_TILINGS:
+                out.append(one(ws, config, label))
+    return out
+
+
+def out_dt_in(w):
+    import torch
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}[w.in_dtype]
 
 
 if __name__ == "__main__":

@@ -85,16 +85,21 @@ enum {
                             or an unknown epilogue */
     SG_ERR_STAGES = -3,  /* stages < 0, > SG_MAX_STAGES, or does not fit in
                             shared memory for the chosen tile */
-    SG_ERR_ALIAS = -4,   /* C overlaps A, B or bias */
-    SG_ERR_ALIGN = -5,   /* A or B not aligned to its 2-byte elements */
+    SG_ERR_ALIAS = -4,   /* C overlaps A, B, R or bias */
+    SG_ERR_ALIGN = -5,   /* a pointer not aligned to its own elements: A or B
+                            (2 bytes for 16-bit operands), C or R (the output
+                            type's size), bias or b_scale (4 bytes) */
     SG_ERR_ARCH = -6,    /* the current device is not sm_103 */
     SG_ERR_CUDA = -7,    /* a CUDA runtime/driver call or the launch failed */
-    SG_ERR_TIMEOUT = -8  /* a device-side wait gave up (reported by
+    SG_ERR_TIMEOUT = -8, /* a device-side wait gave up (reported by
                             sg_device_status) */
+    SG_ERR_CONFIG = -9   /* sg_gemm_ex / sg_plan_ex: an unknown field value,
+                            or a tile width or kernel mode this problem
+                            cannot take */
 };
 
 #define SG_MAX_STAGES 8
-#define SG_VERSION 110 /* 1.1.0: sg_plan_info gained tail_units */
+#define SG_VERSION 120 /* 1.2.0: sg_gemm_ex / sg_plan_ex with sg_config; C and bias alignment checked */
 
 /*
  * sg_gemm -- C[i*ldc + j] = epilogue(sum_k A[i*lda + k] * B[k*ldb + j])
@@ -118,9 +123,10 @@ enum {
  * loads of the producer warp into the same shared-memory layout (slower; the
  * kernel then runs one CTA per tile); the results are bit-identical.  Only
  * element alignment (2 bytes for 16-bit operands) is required, else
- * SG_ERR_ALIGN.  C has no
- * alignment rule: a C that is not 16-byte aligned or whose pitch is not a
- * multiple of 16 bytes gets masked element stores instead of TMA stores.
+ * SG_ERR_ALIGN.  C must be aligned to its own elements (4 bytes for fp32, 2
+ * for fp16 / bf16) and bias to 4 bytes, else SG_ERR_ALIGN; a C that is not
+ * 16-byte aligned or whose pitch is not a multiple of 16 bytes gets masked
+ * element stores instead of TMA stores (slower; the same bits).
  */
 int sg_gemm(int64_t M, int64_t N, int64_t K,
             const void* A, int64_t lda,
@@ -167,7 +173,8 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K,
  * and N <= 512 (else SG_ERR_ARG), and A must be TMA-legal (16-byte aligned
  * base, pitch a multiple of 16 bytes; else SG_ERR_ARG).  The scales must be
  * finite.  C must not overlap A, Bq, b_scale or bias (SG_ERR_ALIAS); a NULL
- * b_scale, or a NULL Bq with K > 0, is SG_ERR_ARG; in_dtype other than
+ * b_scale, or a NULL Bq with K > 0, is SG_ERR_ARG; a b_scale not aligned
+ * to 4 bytes is SG_ERR_ALIGN; in_dtype other than
  * fp16/bf16 is SG_ERR_DTYPE.  Everything else is as for sg_gemm.
  */
 int sg_gemm_qb(int64_t M, int64_t N, int64_t K,
@@ -229,13 +236,12 @@ typedef struct {
     int32_t tma_store;     /* 1: C written by TMA stores, 0: masked stores */
     int32_t cluster_m;     /* CTAs per cluster (1 or 2) */
     int32_t pair_mma;      /* 1: the cluster's two CTAs compute one 256-row tile
-                              with the paired MMA; 0: one CTA per 128-row tile
-                              (with cluster_m 2: the pair shares each B tile by
-                              multicast) */
+                              with the paired MMA, each CTA owning 128 rows of
+                              it; 0: one CTA per 128-row tile */
     int32_t group_m;       /* cluster row blocks swept together by the tile raster */
-    int32_t mode;          /* 1 single CTA, 2 CTA pair sharing B by multicast,
-                              3 paired MMA, 4 B resident in shared memory,
-                              5 integer-coded B decoded into shared memory */
+    int32_t mode;          /* 1 single CTA, 3 paired MMA, 4 B resident in
+                              shared memory, 5 integer-coded B decoded into
+                              shared memory (2 is not used) */
     int32_t ring_group;    /* ring slots filled and consumed together on one
                               pair of barriers (2 when both operands arrive by
                               TMA and the ring has 6 or 8 slots, else 1) */
@@ -248,6 +254,65 @@ typedef struct {
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,
             int64_t ldc, const void* C, sg_plan_info* info);
+
+/*
+ * Launch configuration for sg_gemm_ex and sg_plan_ex.  A field left 0 is the
+ * planner's choice; a non-zero field is honoured exactly or the call fails
+ * with SG_ERR_CONFIG (never silently replaced).  Every configuration issues
+ * the same MMAs in the same K order for each output element, so C has the
+ * same bits whatever the configuration (gizml:tile, "tune": every
+ * configuration computes the same result; Tolk.Stage: staging never rounds).
+ *
+ *   block_n     output tile columns: 128, 192 or 256 (FP8 operands: 128 or
+ *               256, whole 128-byte B boxes).
+ *   mode        1: one CTA per 128 x block_n output tile.
+ *               3: the two CTAs of a cluster compute one 256 x block_n tile
+ *                  with the paired MMA (tcgen05 cta_group::2); each CTA owns
+ *                  128 x block_n of it and stages its own A rows and half of
+ *                  the B columns.  block_n must split into whole B boxes per
+ *                  CTA (128 or 256 for 16-bit operands, 256 for FP8), and A
+ *                  and B must be TMA-legal.
+ *               4: B resident in shared memory (block_n 128; K at most two
+ *                  128-byte stages of K, N at most 512; A and B TMA-legal).
+ *   stages      operand ring depth, 1..SG_MAX_STAGES (0: the deepest that
+ *               fits); a depth that does not fit is SG_ERR_STAGES.
+ *   group_m     tile raster: cluster row blocks swept together, 1..64.
+ *   tail_split  1 or 0: split a short last wave of 256-column tiles into
+ *               128-column units where it pays (the default); -1: never.
+ *
+ * The gizml:tile program's workgroup per 128 x 128 output tile is
+ * {block_n = 128, mode = 1} (one CTA per tile) or {block_n = 128, mode = 3}
+ * (each CTA of a pair owns one 128 x 128 tile and the pair shares B).
+ */
+typedef struct {
+    int32_t block_n;
+    int32_t mode;
+    int32_t stages;
+    int32_t group_m;
+    int32_t tail_split;
+} sg_config;
+
+/*
+ * sg_gemm_ex -- sg_gemm (R == NULL) or sg_gemm_residual (R != NULL, with its
+ * rules for R and ldr) under an explicit launch configuration.  `config` may
+ * be NULL or all zeros: then this is exactly sg_gemm / sg_gemm_residual
+ * (including a configuration cached by sg_tune).  Returns sg_gemm's codes,
+ * plus SG_ERR_CONFIG when a requested field cannot be honoured for this
+ * problem (checked on the host before any GPU work is queued).
+ */
+int sg_gemm_ex(int64_t M, int64_t N, int64_t K,
+               const void* A, int64_t lda,
+               const void* B, int64_t ldb,
+               const void* R, int64_t ldr,
+               void* C, int64_t ldc,
+               int in_dtype, int out_dtype, int epilogue,
+               const float* bias, const sg_config* config, void* stream);
+
+/* The launch configuration sg_gemm_ex would use for TMA-legal A and B under
+ * `config` (NULL: sg_plan's), without queueing GPU work.  Needs a current
+ * CUDA device; returns sg_gemm_ex's codes. */
+int sg_plan_ex(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue,
+               int64_t ldc, const void* C, const sg_config* config, sg_plan_info* info);
 
 /*
  * sg_tune -- times every launch configuration that fits this problem (tile

@@ -39,13 +39,11 @@ int sg_test_set_tile_n(int bn);
 
 /*
  * Forces the kernel mode of later sg_gemm / sg_plan calls: 1 (one CTA per
- * 128-row tile, copying its whole B tile), 2 (two CTAs with vertically
- * adjacent tiles share each B tile through TMA multicast) or 3 (the two CTAs
- * of a cluster compute one 256-row tile with the paired MMA, each staging
- * half of B) or 4 (each CTA keeps all of B in shared memory and streams A;
- * only where B has at most 2 K chunks and 4 column blocks of 128, otherwise
- * the planner's choice stands); modes 2 and 3 need a tile width of 128 or
- * 256.  0 restores the planner's choice.  Every mode sums the same products in the same K order
+ * 128-row tile, copying its whole B tile), 3 (the two CTAs of a cluster
+ * compute one 256-row tile with the paired MMA, each staging half of B) or
+ * 4 (each CTA keeps all of B in shared memory and streams A; only where B
+ * has at most 2 K chunks and 4 column blocks of 128, otherwise the
+ * planner's choice stands); mode 3 needs a tile width of 128 or 256.  0 restores the planner's choice.  Every mode sums the same products in the same K order
  * for each output element, so C must be bit-identical.  Returns 0, or
  * SG_ERR_ARG.  The environment variable STAGE_GEMM_CLUSTER sets the initial
  * value at load.

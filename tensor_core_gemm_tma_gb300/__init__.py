@@ -29,7 +29,7 @@ SG_MAX_STAGES = 8
 
 ERRORS = {
     -1: "SG_ERR_ARG", -2: "SG_ERR_DTYPE", -3: "SG_ERR_STAGES", -4: "SG_ERR_ALIAS",
-    -5: "SG_ERR_ALIGN", -6: "SG_ERR_ARCH", -7: "SG_ERR_CUDA", -8: "SG_ERR_TIMEOUT",
+    -5: "SG_ERR_ALIGN", -6: "SG_ERR_ARCH", -7: "SG_ERR_CUDA", -8: "SG_ERR_TIMEOUT", -9: "SG_ERR_CONFIG",
 }
 
 
@@ -48,6 +48,25 @@ class PlanInfo(ctypes.Structure):
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class Config(ctypes.Structure):
+    """sg_config: an explicit launch configuration (0 = the planner's choice
+    for that field).  block_n 128/192/256; mode 1 (one CTA per tile), 3 (CTA
+    pairs with the paired MMA, each CTA owning 128 x block_n) or 4 (resident
+    B); stages 1..8; group_m 1..64; tail_split -1 (never) or 0/1 (default)."""
+    _fields_ = [(n, ctypes.c_int32) for n in ("block_n", "mode", "stages", "group_m", "tail_split")]
+
+
+def _config(config):
+    if config is None:
+        return None
+    if isinstance(config, Config):
+        return config
+    unknown = set(config) - {n for n, _ in Config._fields_}
+    if unknown:
+        raise ValueError(f"unknown configuration fields {sorted(unknown)}")
+    return Config(**{k: int(v) for k, v in config.items()})
 
 
 _lock = threading.Lock()
@@ -78,6 +97,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.sg_gemm_host.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp, i32, vp]
         lib.sg_plan.restype = i32
         lib.sg_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i64, vp, ctypes.POINTER(PlanInfo)]
+        lib.sg_gemm_ex.restype = i32
+        lib.sg_gemm_ex.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, vp,
+                                   ctypes.POINTER(Config), vp]
+        lib.sg_plan_ex.restype = i32
+        lib.sg_plan_ex.argtypes = [i64, i64, i64, i32, i32, i32, i64, vp, ctypes.POINTER(Config),
+                                   ctypes.POINTER(PlanInfo)]
         lib.sg_device_status.restype = i32
         lib.sg_device_status.argtypes = [vp]
         lib.sg_set_wait_limit_ns.restype = None
@@ -169,7 +194,7 @@ def gemm_raw(M: int, N: int, K: int, A_ptr: int, lda: int, B_ptr: int, ldb: int,
 
 
 def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: int = 0, out=None, stream=None,
-               residual=None):
+               residual=None, config=None):
     """C = epilogue(A @ B [+ residual]) on A's CUDA device, queued on
     ``stream`` (default: the current stream).  A (M x K) and B (K x N) are
     row-major fp16 or bf16 CUDA tensors of one dtype; ``out_dtype`` is
@@ -178,7 +203,12 @@ def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: 
     row-major tensor of the output dtype added to the accumulator before the
     bias and the ReLU (it may be ``out`` itself); ``stages`` is the operand
     ring depth (0: the largest that fits).  ``out`` may be a preallocated
-    row-major M x N view (its padding columns are never written)."""
+    row-major M x N view (its padding columns are never written).
+    ``config`` (a dict of sg_config fields or a ``Config``) fixes the launch
+    configuration through sg_gemm_ex: e.g. ``{"block_n": 128, "mode": 3}``
+    runs 128 x 128 output tiles per CTA, CTA pairs sharing B; a field the
+    problem cannot take raises SG_ERR_CONFIG.  Every configuration gives the
+    same bits."""
     torch = _torch()
     if A.device.type != "cuda" or B.device.type != "cuda":
         raise ValueError("A and B must be CUDA tensors")
@@ -204,6 +234,16 @@ def stage_gemm(A, B, out_dtype=None, epilogue: str = "none", bias=None, stages: 
     if residual is not None:
         if residual.dtype != out.dtype or tuple(residual.shape) != (M, N) or residual.device != A.device:
             raise ValueError("residual must be an M x N CUDA tensor of the output dtype")
+    if config is not None:
+        cfg = _config(config)
+        if stages:
+            cfg.stages = int(stages)
+        rptr, ldr = (None, 0) if residual is None else (residual.data_ptr(), _row_pitch(residual))
+        rc = load_library().sg_gemm_ex(
+            M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), rptr, ldr, out.data_ptr(),
+            _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype), EPILOGUES[epilogue], bptr,
+            ctypes.byref(cfg), _stream_ptr(stream, A.device).value)
+    elif residual is not None:
         rc = load_library().sg_gemm_residual(
             M, N, K, A.data_ptr(), _row_pitch(A), B.data_ptr(), _row_pitch(B), residual.data_ptr(),
             _row_pitch(residual), out.data_ptr(), _row_pitch(out), dtype_code(A.dtype), dtype_code(out.dtype),
@@ -306,12 +346,21 @@ def stage_gemm_host(A_host, B_host, out_dtype=None, epilogue: str = "none", bias
 
 
 def plan(M: int, N: int, K: int, in_dtype, out_dtype, epilogue: str = "none", stages: int = 0, ldc: int | None = None,
-         C_ptr: int = 0) -> dict:
+         C_ptr: int = 0, config=None) -> dict:
     """The launch configuration ``stage_gemm`` would use (tile, stages, grid,
-    shared memory).  Needs a CUDA device."""
+    shared memory), under ``config`` if given (sg_plan_ex).  Needs a CUDA
+    device."""
     info = PlanInfo()
-    rc = load_library().sg_plan(M, N, K, dtype_code(in_dtype), dtype_code(out_dtype), EPILOGUES[epilogue],
-                                int(stages), N if ldc is None else ldc, C_ptr, ctypes.byref(info))
+    ldc = N if ldc is None else ldc
+    if config is not None:
+        cfg = _config(config)
+        if stages:
+            cfg.stages = int(stages)
+        rc = load_library().sg_plan_ex(M, N, K, dtype_code(in_dtype), dtype_code(out_dtype), EPILOGUES[epilogue],
+                                       ldc, C_ptr, ctypes.byref(cfg), ctypes.byref(info))
+    else:
+        rc = load_library().sg_plan(M, N, K, dtype_code(in_dtype), dtype_code(out_dtype), EPILOGUES[epilogue],
+                                    int(stages), ldc, C_ptr, ctypes.byref(info))
     _check(rc)
     return info.as_dict()
 

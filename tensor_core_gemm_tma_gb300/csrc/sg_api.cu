@@ -110,11 +110,29 @@ int check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
             return SG_ERR_ALIAS;
     }
     if (bias && overlap(C, c_span, bias, static_cast<uint64_t>(N) * 4)) return SG_ERR_ALIAS;
-    // 16-bit elements must sit on 2-byte boundaries; anything coarser is
-    // handled (TMA when legal, element loads otherwise)
+    // Every pointer must sit on a boundary of its own elements (2 bytes for
+    // 16-bit operands, the output type's size for C, 4 for the fp32 bias):
+    // the element loads and masked element stores that take over where TMA
+    // cannot address an operand or C access single elements, and a
+    // misaligned element access faults on the GPU.  Anything coarser is
+    // handled (TMA when legal, element accesses otherwise).
     const uintptr_t emask = static_cast<uintptr_t>(elem_bytes(in_dtype) - 1);
     if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & emask) || (reinterpret_cast<uintptr_t>(B) & emask)))
         return SG_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(C) & static_cast<uintptr_t>(elem_bytes(out_dtype) - 1)) return SG_ERR_ALIGN;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) return SG_ERR_ALIGN;
+    return SG_OK;
+}
+
+// The residual's host-only checks (sg_gemm_residual, sg_gemm_ex, sg_gemm_host).
+int check_residual(int64_t M, int64_t N, const void* R, int64_t ldr, const void* C, int64_t ldc, int out_dtype) {
+    if (!R || ldr < N || ldr > 0x7FFFFFFF) return SG_ERR_ARG;
+    const int oes = elem_bytes(out_dtype);
+    if (reinterpret_cast<uintptr_t>(R) % oes) return SG_ERR_ALIGN;
+    // R may be C itself (each element is read before it is written); any
+    // other overlap of the two would race
+    const bool same = (R == C && ldr == ldc);
+    if (!same && overlap(C, span_bytes(M, N, ldc, oes), R, span_bytes(M, N, ldr, oes))) return SG_ERR_ALIAS;
     return SG_OK;
 }
 
@@ -203,10 +221,14 @@ int64_t host_chunk_rows(int64_t M, uint64_t copy_bytes) {
     return std::max<int64_t>(rows, 1);
 }
 
-// A launch configuration chosen by sg_tune (or forced): every field
-// non-zero overrides the planner's heuristic.
+// A launch configuration chosen by sg_tune or given to sg_gemm_ex: every
+// non-zero field overrides the planner's heuristic.  tail_split < 0 never
+// splits the last wave.  A strict choice (sg_gemm_ex) must be honoured as
+// given: a tile width or mode the problem cannot take is SG_ERR_CONFIG
+// instead of the planner's fallback.
 struct Choice {
-    int bn = 0, mode = 0, stages = 0, group_m = 0;
+    int bn = 0, mode = 0, stages = 0, group_m = 0, tail_split = 0;
+    bool strict = false;
 };
 
 // Tuning cache: the fastest configuration measured for each problem key.
@@ -222,7 +244,7 @@ struct Plan {
     int bn = 128;
     int block_k = 64;  // K elements per stage (128 bytes of K)
     int group_m = 12;
-    int mode = 1;  // 1: single CTA, 2: CTA pairs sharing B by multicast, 3: paired MMA
+    int mode = 1;  // 1: single CTA, 3: paired MMA, 4: resident B, 5: decoded panel
     int cm = 1;    // CTAs per cluster along M
     int stages = 0, max_stages = 0;
     int ring_group = 1;  // ring slots sharing one full and one empty barrier
@@ -280,12 +302,13 @@ std::atomic<int> g_tail_split{[] {
 }()};
 
 // Kernel mode forced by sg_test_set_cluster or, at load, the environment
-// variable STAGE_GEMM_CLUSTER (1: single CTA, 2: CTA pairs sharing B by
-// multicast, 3: paired MMA, 4: resident B; 0: the planner's choice).
+// variable STAGE_GEMM_CLUSTER (1: single CTA, 3: paired MMA, 4: resident B;
+// 0: the planner's choice).
+bool valid_mode(int x) { return x == 1 || x == 3 || x == 4; }
 std::atomic<int> g_force_mode{[] {
     const char* e = std::getenv("STAGE_GEMM_CLUSTER");
     const int x = e ? std::atoi(e) : 0;
-    return (x >= 1 && x <= 4) ? x : 0;
+    return valid_mode(x) ? x : 0;
 }()};
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, const void* C,
@@ -324,6 +347,8 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     }
     if (forced_bn()) bn = forced_bn();
     if (choice && choice->bn) bn = choice->bn;
+    const bool bn_forced = forced_bn() || (choice && choice->bn);
+    if (bn % boxc) return SG_ERR_CONFIG;  // a forced width that is not whole 128-byte B boxes
     pl->bn = bn;
     pl->group_m = (choice && choice->group_m) ? choice->group_m : kGroupM;
     pl->n_blocks = cdiv(N, bn);
@@ -339,8 +364,8 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     const int64_t nb128 = cdiv(N, 128);
     const bool panel_ok = a_tma && b_tma && pl->k_chunks <= 2 && nb128 <= 4 &&
                           smem_panel(128, 2, pl->k_chunks, nb128) <= st.smem_optin;
-    if (panel_ok && pl->m_blocks >= st.sm_count && !forced_bn()) mode = 4;
-    auto legal = [&](int m) { return m == 1 || ((m == 2 || m == 3) && pairable) || (m == 4 && panel_ok); };
+    if (panel_ok && pl->m_blocks >= st.sm_count && !bn_forced) mode = 4;
+    auto legal = [&](int m) { return m == 1 || (m == 3 && pairable) || (m == 4 && panel_ok); };
     if (const int f = g_force_mode.load(); f && legal(f)) mode = f;
     if (choice && choice->mode && legal(choice->mode)) mode = choice->mode;
     if (!a_tma || !b_tma) mode = 1;  // element-load staging runs in single-CTA mode
@@ -359,7 +384,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
         pl->n_blocks = nb128;
     }
     pl->mode = mode;
-    pl->cm = (mode == 2 || mode == 3) ? 2 : 1;
+    pl->cm = mode == 3 ? 2 : 1;
     const int cm = pl->cm;
     // work units handed out by the persistent loop: cluster tiles (modes 1-3)
     // or row tiles covering every column block (modes 4, 5)
@@ -400,7 +425,8 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // unit, summing the same products in the same K order: C keeps its bits.
     pl->units = pl->full_units = pl->tiles;
     const int64_t tail = pl->tiles % clusters;
-    if (g_tail_split.load() && !panel && esz == 2 && bn == 256 && a_tma && b_tma && pl->k_chunks > 0 &&
+    const bool split_ok = g_tail_split.load() && !(choice && choice->tail_split < 0);
+    if (split_ok && !panel && esz == 2 && bn == 256 && a_tma && b_tma && pl->k_chunks > 0 &&
         pl->tiles > clusters && tail > 0 && 2 * tail <= clusters) {
         pl->full_units = pl->tiles - tail;
         pl->units = pl->full_units + 2 * tail;
@@ -512,6 +538,11 @@ bool lookup_tuned(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, 
     return true;
 }
 
+// A plan gives what a strict choice asked for.
+bool honours(const Plan& pl, const Choice& c) {
+    return (!c.bn || pl.bn == c.bn) && (!c.mode || pl.mode == c.mode);
+}
+
 // Plan, build the tensor maps and kernel parameters, and launch (shared by
 // the entry points; `st` supplies the device's attributes and status word).
 // With Bq (mode 5) B is int8 codes with per-column scales b_scale, decoded
@@ -533,6 +564,7 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     Plan pl;
     int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice, decode);
     if (rc != SG_OK) return rc;
+    if (choice && choice->strict && !honours(pl, *choice)) return SG_ERR_CONFIG;
     if (used) *used = pl;
 
     alignas(64) CUtensorMap ta, tb, tc, tr;
@@ -615,13 +647,7 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda
     int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
     if (rc != SG_OK) return rc;
     if (M == 0 || N == 0) return SG_OK;
-    if (!R || ldr < N || ldr > 0x7FFFFFFF) return SG_ERR_ARG;
-    const int oes = elem_bytes(out_dtype);
-    if (reinterpret_cast<uintptr_t>(R) % oes) return SG_ERR_ALIGN;
-    // R may be C itself (each element is read before it is written); any
-    // other overlap of the two would race
-    const bool same = (R == C && ldr == ldc);
-    if (!same && overlap(C, span_bytes(M, N, ldc, oes), R, span_bytes(M, N, ldr, oes))) return SG_ERR_ALIAS;
+    if ((rc = check_residual(M, N, R, ldr, C, ldc, out_dtype)) != SG_OK) return rc;
     DevState* st = nullptr;
     if ((rc = device_state(&st)) != SG_OK) return rc;
     return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
@@ -637,6 +663,7 @@ int sg_gemm_qb(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, cons
     if (rc != SG_OK) return rc;
     if (M == 0 || N == 0) return SG_OK;
     if (!b_scale || ldb > 0x7FFFFFFF) return SG_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(b_scale) & 3u) return SG_ERR_ALIGN;
     if (K > 0 && (!Bq || ldb < N)) return SG_ERR_ARG;
     const uint64_t c_span = span_bytes(M, N, ldc, elem_bytes(out_dtype));
     if ((K > 0 && overlap(C, c_span, Bq, span_bytes(K, N, ldb, 1))) ||
@@ -658,12 +685,7 @@ int sg_gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
     if (rc != SG_OK) return rc;
     if (M == 0 || N == 0) return SG_OK;
     const int esz = elem_bytes(in_dtype), oes = elem_bytes(out_dtype);
-    if (R) {
-        if (ldr < N || ldr > 0x7FFFFFFF) return SG_ERR_ARG;
-        if (reinterpret_cast<uintptr_t>(R) % oes) return SG_ERR_ALIGN;
-        const bool same = (R == C && ldr == ldc);
-        if (!same && overlap(C, span_bytes(M, N, ldc, oes), R, span_bytes(M, N, ldr, oes))) return SG_ERR_ALIAS;
-    }
+    if (R && (rc = check_residual(M, N, R, ldr, C, ldc, out_dtype)) != SG_OK) return rc;
     DevState* st = nullptr;
     if ((rc = device_state(&st)) != SG_OK) return rc;
     if ((rc = host_streams(*st)) != SG_OK) return rc;
@@ -781,6 +803,68 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
     return SG_OK;
 }
 
+// The launch configuration an sg_config asks for, validated on the host.
+static int config_choice(const sg_config* cfg, Choice* c, int* stages) {
+    const sg_config z = {};
+    const sg_config& g = cfg ? *cfg : z;
+    if (g.block_n != 0 && !valid_bn(g.block_n)) return SG_ERR_CONFIG;
+    if (g.mode != 0 && !valid_mode(g.mode)) return SG_ERR_CONFIG;
+    if (g.group_m < 0 || g.group_m > 64 || g.tail_split < -1 || g.tail_split > 1) return SG_ERR_CONFIG;
+    if (g.stages < 0 || g.stages > SG_MAX_STAGES) return SG_ERR_STAGES;
+    c->bn = g.block_n;
+    c->mode = g.mode;
+    c->group_m = g.group_m;
+    c->tail_split = g.tail_split;
+    c->strict = true;
+    *stages = g.stages;
+    // all zeros: exactly sg_gemm (a tuned configuration still applies)
+    return (g.block_n || g.mode || g.group_m || g.tail_split) ? 1 : 0;
+}
+
+int sg_gemm_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+               const void* R, int64_t ldr, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue,
+               const float* bias, const sg_config* config, void* stream) {
+    Choice c;
+    int stages = 0;
+    const int given = config_choice(config, &c, &stages);
+    if (given < 0) return given;
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages);
+    if (rc != SG_OK) return rc;
+    if (M == 0 || N == 0) return SG_OK;
+    if (R && (rc = check_residual(M, N, R, ldr, C, ldc, out_dtype)) != SG_OK) return rc;
+    DevState* st = nullptr;
+    if ((rc = device_state(&st)) != SG_OK) return rc;
+    return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                           g_skip_load.load(), static_cast<cudaStream_t>(stream), given ? &c : nullptr, nullptr, R,
+                           R ? ldr : 0);
+}
+
+int sg_plan_ex(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int64_t ldc,
+               const void* C, const sg_config* config, sg_plan_info* info) {
+    if (!info) return SG_ERR_ARG;
+    std::memset(info, 0, sizeof(*info));
+    Choice c;
+    int stages = 0;
+    const int given = config_choice(config, &c, &stages);
+    if (given < 0) return given;
+    if (!valid_in(in_dtype) || !valid_out(out_dtype) || !valid_epi(epilogue)) return SG_ERR_DTYPE;
+    if (M < 0 || N < 0 || K < 0 || ldc < N) return SG_ERR_ARG;
+    DevState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != SG_OK) return rc;
+    Choice tuned;
+    const Choice* choice = given ? &c : nullptr;
+    if (!choice && lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, true, true, c_tma_legal(C, M, ldc, out_dtype),
+                                &tuned))
+        choice = &tuned;
+    Plan pl;
+    if ((rc = make_plan(*st, M, N, K, in_dtype, out_dtype, C, ldc, stages, true, true, &pl, choice)) != SG_OK)
+        return rc;
+    if (given && !honours(pl, c)) return SG_ERR_CONFIG;
+    fill_info(pl, info);
+    return SG_OK;
+}
+
 int sg_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
             int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias, void* stream,
             sg_plan_info* best, float* best_ms) {
@@ -800,8 +884,8 @@ int sg_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
     for (int bn : {128, 192, 256}) {
         if (bn % (128 / esz)) continue;  // whole 128-byte B boxes
         if (bn > 128 && N <= bn - 64) continue;  // a tile mostly past N
-        for (int mode : {1, 2, 3}) {
-            if (mode > 1 && ((bn / (128 / esz)) % 2 != 0 || m_blocks < 2 || !a_tma || !b_tma)) continue;
+        for (int mode : {1, 3}) {
+            if (mode == 3 && ((bn / (128 / esz)) % 2 != 0 || m_blocks < 2 || !a_tma || !b_tma)) continue;
             for (int g : {4, 8, 12, 16}) {
                 Choice c;
                 c.bn = bn;
@@ -900,11 +984,12 @@ const char* sg_strerror(int code) {
         case SG_ERR_ARG: return "invalid argument (size, leading dimension, pointer or bias)";
         case SG_ERR_DTYPE: return "unsupported storage type or epilogue";
         case SG_ERR_STAGES: return "stage count out of range or does not fit in shared memory";
-        case SG_ERR_ALIAS: return "C overlaps A, B or bias";
-        case SG_ERR_ALIGN: return "A/B base or leading dimension not 16-byte aligned for TMA";
+        case SG_ERR_ALIAS: return "C overlaps A, B, R or bias";
+        case SG_ERR_ALIGN: return "an operand, C, R, bias or scale base not aligned to its element size";
         case SG_ERR_ARCH: return "current device is not sm_103 (GB300)";
         case SG_ERR_CUDA: return "CUDA runtime or driver error";
         case SG_ERR_TIMEOUT: return "a device-side wait gave up";
+        case SG_ERR_CONFIG: return "the requested launch configuration does not fit this problem";
         default: return "unknown error code";
     }
 }
@@ -926,7 +1011,7 @@ int sg_test_set_tile_n(int bn) {
 }
 
 int sg_test_set_cluster(int mode) {
-    if (mode < 0 || mode > 4) return SG_ERR_ARG;
+    if (mode != 0 && !valid_mode(mode)) return SG_ERR_ARG;
     g_force_mode.store(mode);
     return SG_OK;
 }
@@ -997,7 +1082,8 @@ int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's word: clear it for this call
     if (cudaMemsetAsync(st->status, 0, sizeof(int), s) != cudaSuccess) return SG_ERR_CUDA;
-    return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages, -1, s);
+    return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                           g_skip_load.load(), s);
 }
 
 int sg_gemm_noalloc_status(void* stream) {

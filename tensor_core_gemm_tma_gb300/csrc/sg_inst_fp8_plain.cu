@@ -7,15 +7,12 @@ LaunchFn launcher_fp8_plain(int bn, int out, int mode) {
     switch ((bn * 4 + out) * 4 + mode) {
         case (128 * 4 + SG_F32) * 4 + 1: return &launch_kernel<128, SG_F32, 1, false, 1>;
         case (256 * 4 + SG_F32) * 4 + 1: return &launch_kernel<256, SG_F32, 1, false, 1>;
-        case (256 * 4 + SG_F32) * 4 + 2: return &launch_kernel<256, SG_F32, 2, false, 1>;
         case (256 * 4 + SG_F32) * 4 + 3: return &launch_kernel<256, SG_F32, 3, false, 1>;
         case (128 * 4 + SG_F16) * 4 + 1: return &launch_kernel<128, SG_F16, 1, false, 1>;
         case (256 * 4 + SG_F16) * 4 + 1: return &launch_kernel<256, SG_F16, 1, false, 1>;
-        case (256 * 4 + SG_F16) * 4 + 2: return &launch_kernel<256, SG_F16, 2, false, 1>;
         case (256 * 4 + SG_F16) * 4 + 3: return &launch_kernel<256, SG_F16, 3, false, 1>;
         case (128 * 4 + SG_BF16) * 4 + 1: return &launch_kernel<128, SG_BF16, 1, false, 1>;
         case (256 * 4 + SG_BF16) * 4 + 1: return &launch_kernel<256, SG_BF16, 1, false, 1>;
-        case (256 * 4 + SG_BF16) * 4 + 2: return &launch_kernel<256, SG_BF16, 2, false, 1>;
         case (256 * 4 + SG_BF16) * 4 + 3: return &launch_kernel<256, SG_BF16, 3, false, 1>;
         default: return nullptr;
     }

@@ -26,13 +26,8 @@
 //               TMA store that does not write elements outside M x N
 //               (gizml:tile, "Out.put").
 //
-// Five modes (MODE):
+// Four modes (MODE; the numbers are those of sg_plan_info.mode):
 //   1  one CTA per 128 x BN tile.
-//   2  clusters of two CTAs with vertically adjacent 128 x BN tiles and the
-//      same column block: each CTA copies half of the B tile's 64-column
-//      boxes and multicasts them into both CTAs' rings, halving the B
-//      traffic from L2; a ring slot is free only when both CTAs' MMAs have
-//      read it (the empty barrier counts one commit from each CTA).
 //   4  resident B ("decoded panels", Tolk.Stage): for a small K x N, each
 //      CTA stages all of B once (every K chunk of every 128-column block)
 //      and streams only A, one 128-row tile per ring slot; the MMAs of
@@ -530,8 +525,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const Params p) {
-    static_assert(MODE >= 1 && MODE <= 5, "mode 1 to 5");
-    constexpr int CM = (MODE == 2 || MODE == 3) ? 2 : 1;  // CTAs per cluster
+    static_assert(MODE == 1 || MODE == 3 || MODE == 4 || MODE == 5, "modes 1, 3, 4 and 5");
+    constexpr int CM = (MODE == 3) ? 2 : 1;  // CTAs per cluster
     constexpr bool PANEL = (MODE == 4 || MODE == 5);      // B resident in shared memory
     constexpr bool DECODE = (MODE == 5);                  // ... decoded there from int8 codes
     static_assert(!DECODE || (ESZ == 2 && !RES), "mode 5: 16-bit A, no residual");
@@ -541,7 +536,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     using L = Layout<BN, BL>;
     using G = Geom<ESZ>;
     static_assert(BL % G::BOXC == 0, "B is staged in whole 128-byte-wide boxes");
-    static_assert((BL / 64) % (MODE == 2 ? 2 : 1) == 0, "each CTA of a cluster copies whole B boxes");
     constexpr uint16_t CLUSTER_MASK = static_cast<uint16_t>((1u << CM) - 1u);
     const uint32_t rank = (CM > 1) ? cluster_ctarank() : 0u;
     const int cluster_id = static_cast<int>(blockIdx.x) / CM;
@@ -589,7 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), MODE == 2 ? 2 : 1);  // mode 2: one MMA commit from each CTA
+            mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < ACC; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -615,7 +609,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish<CG>();
     }
     tc_fence_before();
-    // the peer's barriers must be initialised before any multicast reaches them
+    // the peer's barriers must be initialised before any copy or commit of the pair reaches them
     if constexpr (CM > 1) {
         cluster_sync();
     } else {
@@ -696,8 +690,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int mb = tile, col0 = 0, width = BN;
                 if constexpr (!PANEL) width = unit_coords<CM, BN, ESZ>(tile, p, rank, mb, col0);
                 // B columns landing in this CTA per K chunk: the paired MMA stages
-                // half of the unit's columns in each CTA; mode 2 multicasts every
-                // box into both CTAs
+                // half of the unit's columns in each CTA
                 const int bl = PAIR ? width / 2 : width;
                 const uint32_t chunk_tx = A_STAGE_BYTES + static_cast<uint32_t>(bl) * BK_BYTES;
                 const int fills = PANEL ? 1 : p.k_chunks;  // mode 4: one ring slot holds every K chunk of A
@@ -733,15 +726,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 const uint32_t sc = sa + c * stage_bytes;
                                 const int k0 = (kc + c) * G::KB;
                                 tma_load_2d(sc, &tmA, full_bar(slot), k0, mb * BM);
-                                for (int j = 0; j < width / G::BOXC; ++j) {
-                                    const uint32_t dst = sc + A_STAGE_BYTES + j * G::B_BOX_BYTES;
-                                    if constexpr (MODE == 1) {
-                                        tma_load_2d(dst, &tmB, full_bar(slot), col0 + j * G::BOXC, k0);
-                                    } else if (j % 2 == static_cast<int>(rank)) {
-                                        tma_load_2d_multicast(dst, &tmB, full_bar(slot), col0 + j * G::BOXC, k0,
-                                                              CLUSTER_MASK);
-                                    }
-                                }
+                                for (int j = 0; j < width / G::BOXC; ++j)
+                                    tma_load_2d(sc + A_STAGE_BYTES + j * G::B_BOX_BYTES, &tmB, full_bar(slot),
+                                                col0 + j * G::BOXC, k0);
                             }
                         }
                         issued |= 1u << slot;
@@ -867,12 +854,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 }
                             }
                         }
-                        if constexpr (MODE == 1 || MODE == 4) {
-                            umma_commit(empty_bar(slot));
-                        } else if constexpr (MODE == 2) {
-                            umma_commit_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slots in both CTAs
+                        if constexpr (PAIR) {
+                            umma_commit_pair_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slots in both CTAs
                         } else {
-                            umma_commit_pair_multicast(empty_bar(slot), CLUSTER_MASK);
+                            umma_commit(empty_bar(slot));
                         }
                     }
                     slot += ring_group;
@@ -1086,7 +1071,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     __syncwarp();  // lanes that skipped a lane-0 role wait for it here
     tc_fence_before();
-    // no CTA leaves while its peer may still multicast into it or arrive on it
+    // no CTA leaves while its peer may still copy into it or arrive on it
     if constexpr (CM > 1) {
         cluster_sync();
     } else {

@@ -35,7 +35,7 @@ using LaunchFn = int (*)(LaunchArgs&);
 
 template <int BN, int OUT, int MODE, bool RES, int ESZ>
 int launch_kernel(LaunchArgs& a) {
-    constexpr int CM = (MODE == 2 || MODE == 3) ? 2 : 1;  // CTAs per cluster
+    constexpr int CM = (MODE == 3) ? 2 : 1;  // CTAs per cluster
     auto kern = sg_gemm_kernel<BN, OUT, MODE, RES, ESZ>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -79,10 +79,10 @@ int launch_kernel(LaunchArgs& a) {
 // The launcher of one instantiation, or nullptr if it does not exist.
 // Defined by the instantiation units.  16-bit operands:
 LaunchFn launcher_plain_single(int bn, int out);  // mode 1, no residual
-LaunchFn launcher_plain_pair(int bn, int out, int mode);  // modes 2 and 3, no residual
+LaunchFn launcher_plain_pair(int bn, int out, int mode);  // mode 3 (paired MMA), no residual
 LaunchFn launcher_res_single(int bn, int out);
 LaunchFn launcher_res_pair(int bn, int out, int mode);
-// FP8 E4M3 operands (tile widths 128 and 256; pairs only at 256):
+// FP8 E4M3 operands (tile widths 128 and 256; the paired MMA only at 256):
 LaunchFn launcher_fp8_plain(int bn, int out, int mode);
 LaunchFn launcher_fp8_res(int bn, int out, int mode);
 // Mode 4 (resident B), tile width 128, either element size (esz 1 or 2):

@@ -86,18 +86,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
-// The same load delivered to the same shared-memory offset of every CTA of
-// the cluster in `mask`, completing bytes on the barrier at the same offset
-// in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, uint32_t bar, int32_t x,
-                                                      int32_t y, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-        : "memory");
-}
-
 // 2-D tiled store shared -> global.  Elements outside the tensor map's
 // extents are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
@@ -267,15 +255,6 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// As umma_commit, arriving on the barrier at the same offset in every CTA of
-// the cluster in `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-        ::"r"(bar), "h"(mask)
-        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives

@@ -44,8 +44,8 @@ def test_library_exports_every_declared_symbol(sg):
 
 
 def test_version_and_strerror(sg):
-    assert sg.version() == 110
-    for code in range(0, -9, -1):
+    assert sg.version() == 120
+    for code in range(0, -10, -1):
         txt = sg.strerror(code)
         assert txt and txt != "unknown error code"
     assert sg.strerror(-99) == "unknown error code"
@@ -135,6 +135,42 @@ def test_rejects_element_misalignment(sg):
     # staged by element loads and needs a GPU, so it is tested there)
     assert call(sg, A=P16 + 1) == -5
     assert call(sg, B=P16B + 3) == -5
+
+
+@needs_no_gpu
+def test_rejects_c_and_bias_misalignment(sg):
+    # C off its own elements (4 bytes for fp32, 2 for fp16) and a bias off
+    # 4 bytes would make the masked element stores / scalar bias loads fault
+    # on the GPU: rejected on the host
+    assert call(sg, C=PC + 2, outd=0) == -5
+    assert call(sg, C=PC + 1, outd=1) == -5
+    assert call(sg, epi=2, bias=0x7000002) == -5
+
+
+@needs_no_gpu
+def test_config_entry_rejects_bad_configs(sg):
+    """sg_gemm_ex checks its configuration on the host before anything else:
+    unknown tile widths, modes (2 is not a mode), raster groups and tail
+    settings are SG_ERR_CONFIG, an out-of-range depth SG_ERR_STAGES; with a
+    valid configuration the ordinary argument checks follow."""
+    lib = sg.load_library()
+
+    def ex(cfg, M=64, C=PC, lda=64, outd=0):
+        return lib.sg_gemm_ex(M, 64, 64, P16, lda, P16B, 64, None, 0, C, 64, 1, outd, 0, None,
+                              ctypes.byref(sg.Config(**cfg)), None)
+
+    assert ex({"block_n": 64}) == -9
+    assert ex({"block_n": 320}) == -9
+    assert ex({"mode": 2}) == -9
+    assert ex({"mode": 5}) == -9
+    assert ex({"group_m": 65}) == -9
+    assert ex({"tail_split": 2}) == -9
+    assert ex({"stages": 9}) == -3
+    assert ex({"block_n": 128, "mode": 3}, M=0) == 0          # empty: a no-op
+    assert ex({"block_n": 128, "mode": 3}, lda=63) == -1      # then sg_gemm's checks
+    assert ex({"block_n": 128, "mode": 3}, C=PC + 2) == -5
+    with pytest.raises(ValueError):
+        sg._config({"tile": 128})
 
 
 @needs_no_gpu

@@ -52,7 +52,7 @@ def test_fp8_stages_widths_modes_bit_identical():
     a, b = _case(M, N, K, seed=102)
     outs = {}
     try:
-        for bn, modes in ((128, (1,)), (256, (1, 2, 3))):
+        for bn, modes in ((128, (1,)), (256, (1, 3))):
             assert lib.sg_test_set_tile_n(bn) == 0
             for mode in modes:
                 assert lib.sg_test_set_cluster(mode) == 0

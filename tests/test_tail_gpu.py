@@ -50,7 +50,7 @@ class _Hooks:
 CASES = [
     # M, N, K, in, out, epilogue, mode
     (2500, 2300, 300, "f16", "f32", "none", 1),       # 20 x 9 tiles over 152 CTAs: 28 split, ragged M, N, K
-    (2500, 2300, 300, "bf16", "bf16", "relu", 2),     # CTA pairs sharing B: 10 x 9 cluster tiles, 14 split
+    (2500, 2300, 300, "bf16", "bf16", "relu", 1),     # single CTAs, bf16 with ReLU: 28 split
     (2500, 2300, 300, "f16", "f16", "bias_relu", 3),  # paired MMA, 256-row tiles: 14 split
     (2560, 2048, 1024, "bf16", "f32", "none", 3),     # whole tiles: 10 x 8 = 80 over 76 clusters, 4 split
 ]

@@ -56,6 +56,41 @@ def test_noalloc_matches_sg_gemm_twice(M, N, K, in_dt, out_dt, epi):
         got = from_device_bits(C, out_dt)
         compare(got, expected, S, out_dt, f"noalloc vs sg_gemm, call {call}")
         compare(got, ref, S, out_dt, f"noalloc vs oracle, call {call}")
+        # the same plan and kernel as sg_gemm: the same bits, not only within tolerance
+        assert np.array_equal(got, expected), f"call {call}: bits differ from sg_gemm"
+
+
+def test_noalloc_status_records_a_timeout_and_is_cleared():
+    """The status word in the static array records a device-side wait that
+    gave up (a K chunk whose copy a test hook skips, with a 50 ms limit),
+    and the next call clears it before its kernel runs: a clean call then
+    reports 0 and matches the oracle."""
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = _noalloc_lib()
+    M, N, K = 1024, 512, 512
+    a, b = seeded_case(M, N, K, "f16", seed=43)
+    dev = torch.device("cuda")
+    A = to_device_bits(a, "f16", dev)
+    B = to_device_bits(b, "f16", dev)
+    C = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    hooks = sg.load_library()
+    old = sg.get_wait_limit_ns()
+    try:
+        sg.set_wait_limit_ns(50_000_000)
+        hooks.sg_test_set_skip_load(1)
+        assert lib.sg_gemm_noalloc(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, 1, 0, 0, None, 0,
+                                   stream) == 0
+        assert lib.sg_gemm_noalloc_status(stream) == -8      # SG_ERR_TIMEOUT, from the static array
+    finally:
+        hooks.sg_test_set_skip_load(-1)
+        sg.set_wait_limit_ns(old)
+    assert lib.sg_gemm_noalloc(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N, 1, 0, 0, None, 0,
+                               stream) == 0
+    assert lib.sg_gemm_noalloc_status(stream) == 0
+    ref, _, S = oracle.gemm(a, b, "f16", "f32")
+    compare(from_device_bits(C, "f32"), ref, S, "f32", "noalloc after a timeout")
 
 
 def test_noalloc_rejects_like_sg_gemm():
@@ -67,3 +102,5 @@ def test_noalloc_rejects_like_sg_gemm():
     assert lib.sg_gemm_noalloc(64, 64, 64, 0x10001, 64, 0x20000, 64, 0x400000, 64, 1, 0, 0, None, 0, None) == -5
     assert lib.sg_gemm_noalloc(64, 64, 64, 0x10000, 64, 0x20000, 64, 0x400000, 64, 1, 0, 9, None, 0, None) == -2
     assert lib.sg_gemm_noalloc(-1, 64, 64, 0x10000, 64, 0x20000, 64, 0x400000, 64, 1, 0, 0, None, 0, None) == -1
+    # a C off its 4-byte fp32 elements
+    assert lib.sg_gemm_noalloc(64, 64, 64, 0x10000, 64, 0x20000, 64, 0x400002, 64, 1, 0, 0, None, 0, None) == -5
