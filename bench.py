@@ -514,14 +514,20 @@ def library_reference(w, dev_tensors, stream, steps=10, warmup=3, flush_mode="wr
             torch._scaled_mm(A, Bc, scale_a=one, scale_b=one, out_dtype=C.dtype, use_fast_accum=False)
         impl = "torch._scaled_mm (cuBLAS FP8, fp32 accumulation)"
     else:
+        # torch's matmul writes the operands' type only: an fp32-output
+        # product is timed with fp16/bf16 output (the library's nearest form)
+        Cl = C if C.dtype == A.dtype else torch.empty(C.shape, dtype=A.dtype, device=A.device)
+
         def call():
             if w.epilogue == "bias_relu":
-                torch.addmm(bias.to(C.dtype), A, B, out=C)
+                torch.addmm(bias.to(Cl.dtype), A, B, out=Cl)
             else:
-                torch.matmul(A, B, out=C)
+                torch.matmul(A, B, out=Cl)
             if w.epilogue != "none":
-                C.relu_()
+                Cl.relu_()
         impl = "torch.matmul (cuBLAS)" + (" + torch ReLU" if w.epilogue != "none" else "")
+        if Cl is not C:
+            impl += f" with {str(A.dtype).replace('torch.', '')} output (torch has no fp32-output form)"
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
