@@ -44,8 +44,8 @@ struct DevState {
     int major = 0, minor = 0;
     int* status = nullptr;  // device status word (4 bytes, library-owned)
     // per kernel instantiation [tile width][output type][mode - 1][residual]:
-    bool attr_done[2][3][3][5][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
-    int max_clusters[2][3][3][5][2] = {};  // the same index: co-resident clusters (0: not queried)
+    bool attr_done[2][3][3][6][2] = {};    // [8-bit][tile width][output type][mode - 1][residual]: attribute set
+    int max_clusters[2][3][3][6][2] = {};  // the same index: co-resident clusters (0: not queried)
     // sg_gemm_host: library-owned copy streams, a second compute stream and
     // events, created on first use
     cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
@@ -241,10 +241,11 @@ TuneKey tune_key(int dev, int64_t M, int64_t N, int64_t K, int in_dtype, int out
 }
 
 struct Plan {
-    int bn = 128;
+    int bn = 128;      // accumulator width (the MMA's N)
+    int tw = 128;      // tile width: bn, or 2 * bn for mode 6's two accumulators
     int block_k = 64;  // K elements per stage (128 bytes of K)
     int group_m = 12;
-    int mode = 1;  // 1: single CTA, 3: paired MMA, 4: resident B, 5: decoded panel
+    int mode = 1;  // 1: single CTA, 3: paired MMA, 4: resident B, 5: decoded panel, 6: wide paired tiles
     int cm = 1;    // CTAs per cluster along M
     int stages = 0, max_stages = 0;
     int ring_group = 1;  // ring slots sharing one full and one empty barrier
@@ -267,6 +268,9 @@ int64_t smem_panel(int bn, int stages, int64_t k_chunks, int64_t n_blocks, bool 
 }
 
 int smem_for(int bn, int stages, int mode) {
+    if (mode == 6) {  // each CTA stages half of each of the tile's two accumulators' B
+        return bn == 256 ? sg::Layout<256, 256>::smem_bytes(stages) : -1;
+    }
     if (mode == 3) {  // each CTA stages half of B
         switch (bn) {
             case 128: return sg::Layout<128, 64>::smem_bytes(stages);
@@ -302,9 +306,11 @@ std::atomic<int> g_tail_split{[] {
 }()};
 
 // Kernel mode forced by sg_test_set_cluster or, at load, the environment
-// variable STAGE_GEMM_CLUSTER (1: single CTA, 3: paired MMA, 4: resident B;
-// 0: the planner's choice).
-bool valid_mode(int x) { return x == 1 || x == 3 || x == 4; }
+// variable STAGE_GEMM_CLUSTER (1: single CTA, 3: paired MMA, 4: resident B,
+// 6: wide paired tiles; 0: the planner's choice).
+bool valid_mode(int x) { return x == 1 || x == 3 || x == 4 || x == 6; }
+// Tile widths an sg_config may ask for (512: mode 6's two 256-column accumulators).
+bool valid_tile(int x) { return valid_bn(x) || x == 512; }
 std::atomic<int> g_force_mode{[] {
     const char* e = std::getenv("STAGE_GEMM_CLUSTER");
     const int x = e ? std::atoi(e) : 0;
@@ -346,12 +352,20 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
         }
     }
     if (forced_bn()) bn = forced_bn();
-    if (choice && choice->bn) bn = choice->bn;
-    const bool bn_forced = forced_bn() || (choice && choice->bn);
+    // a 512-column tile is mode 6: two 256-column accumulators
+    bool wide = false;
+    if (choice && choice->bn) {
+        wide = choice->bn == 512;
+        bn = wide ? 256 : choice->bn;
+    }
+    if (choice && choice->mode == 6) {
+        wide = true;
+        if (!choice->bn) bn = 256;
+    }
+    const bool bn_forced = forced_bn() || (choice && (choice->bn || choice->mode == 6));
     if (bn % boxc) return SG_ERR_CONFIG;  // a forced width that is not whole 128-byte B boxes
     pl->bn = bn;
     pl->group_m = (choice && choice->group_m) ? choice->group_m : kGroupM;
-    pl->n_blocks = cdiv(N, bn);
     const bool pairable = (bn / boxc) % 2 == 0;  // each CTA of a pair owns whole boxes of B
     // Pairs of CTAs compute 256-row tiles with the paired MMA when the K loop
     // is long enough for operand traffic to matter: each SM then stages only
@@ -365,9 +379,12 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     const bool panel_ok = a_tma && b_tma && pl->k_chunks <= 2 && nb128 <= 4 &&
                           smem_panel(128, 2, pl->k_chunks, nb128) <= st.smem_optin;
     if (panel_ok && pl->m_blocks >= st.sm_count && !bn_forced) mode = 4;
-    auto legal = [&](int m) { return m == 1 || (m == 3 && pairable) || (m == 4 && panel_ok); };
+    auto legal = [&](int m) {
+        return m == 1 || (m == 3 && pairable) || (m == 4 && panel_ok) || (m == 6 && bn == 256 && a_tma && b_tma);
+    };
     if (const int f = g_force_mode.load(); f && legal(f)) mode = f;
     if (choice && choice->mode && legal(choice->mode)) mode = choice->mode;
+    if (wide && legal(6)) mode = 6;
     if (!a_tma || !b_tma) mode = 1;  // element-load staging runs in single-CTA mode
     if (decode) {
         // mode 5: the integer-coded B is decoded into mode 4's resident panel,
@@ -384,9 +401,11 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
         pl->n_blocks = nb128;
     }
     pl->mode = mode;
-    pl->cm = mode == 3 ? 2 : 1;
+    pl->tw = mode == 6 ? 2 * bn : bn;
+    if (!panel) pl->n_blocks = cdiv(N, pl->tw);
+    pl->cm = (mode == 3 || mode == 6) ? 2 : 1;
     const int cm = pl->cm;
-    // work units handed out by the persistent loop: cluster tiles (modes 1-3)
+    // work units handed out by the persistent loop: cluster tiles (modes 1, 3, 6)
     // or row tiles covering every column block (modes 4, 5)
     pl->tiles = panel ? pl->m_blocks : cdiv(pl->m_blocks, cm) * pl->n_blocks;
     int maxs = 0;
@@ -426,7 +445,8 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     pl->units = pl->full_units = pl->tiles;
     const int64_t tail = pl->tiles % clusters;
     const bool split_ok = g_tail_split.load() && !(choice && choice->tail_split < 0);
-    if (split_ok && !panel && esz == 2 && bn == 256 && a_tma && b_tma && pl->k_chunks > 0 &&
+    const bool splittable = mode == 6 || (esz == 2 && bn == 256);  // halves of whole B boxes per CTA
+    if (split_ok && !panel && splittable && a_tma && b_tma && pl->k_chunks > 0 &&
         pl->tiles > clusters && tail > 0 && 2 * tail <= clusters) {
         pl->full_units = pl->tiles - tail;
         pl->units = pl->full_units + 2 * tail;
@@ -469,6 +489,8 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
     sg::LaunchFn fn = nullptr;
     if (pl.mode == 5)
         fn = sg::launcher_decoded(out_dtype);
+    else if (pl.mode == 6)
+        fn = sg::launcher_wide(out_dtype, residual, pl.block_k == sg::BK_BYTES ? 1 : 2);
     else if (pl.mode == 4)
         fn = sg::launcher_panel(out_dtype, residual, pl.block_k == sg::BK_BYTES ? 1 : 2);
     else if (pl.block_k == sg::BK_BYTES)  // 8-bit operands
@@ -500,7 +522,7 @@ int launch_plan(DevState& st, int out_dtype, const Plan& pl, const CUtensorMap& 
 void fill_info(const Plan& pl, sg_plan_info* info) {
     std::memset(info, 0, sizeof(*info));
     info->block_m = sg::BM;
-    info->block_n = pl.bn;
+    info->block_n = pl.tw;
     info->block_k = static_cast<int32_t>(pl.block_k);
     info->stages = pl.stages;
     info->max_stages = pl.max_stages;
@@ -511,7 +533,7 @@ void fill_info(const Plan& pl, sg_plan_info* info) {
     info->tmem_columns = pl.tmem_cols;
     info->tma_store = pl.tma_store;
     info->cluster_m = pl.cm;
-    info->pair_mma = pl.mode == 3 ? 1 : 0;
+    info->pair_mma = (pl.mode == 3 || pl.mode == 6) ? 1 : 0;
     info->group_m = pl.group_m;
     info->mode = pl.mode;
     info->ring_group = pl.ring_group;
@@ -540,7 +562,7 @@ bool lookup_tuned(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, 
 
 // A plan gives what a strict choice asked for.
 bool honours(const Plan& pl, const Choice& c) {
-    return (!c.bn || pl.bn == c.bn) && (!c.mode || pl.mode == c.mode);
+    return (!c.bn || pl.tw == c.bn) && (!c.mode || pl.mode == c.mode);
 }
 
 // Plan, build the tensor maps and kernel parameters, and launch (shared by
@@ -598,7 +620,7 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.stages = pl.stages;
     prm.ring_group = pl.ring_group;
     prm.group_m = pl.group_m;
-    const int mma_m = pl.mode == 3 ? 2 * sg::BM : sg::BM;
+    const int mma_m = (pl.mode == 3 || pl.mode == 6) ? 2 * sg::BM : sg::BM;
     prm.idesc = esz == 1 ? sg::idesc_e4m3(mma_m, pl.bn, true)
                          : sg::idesc_f16(in_dtype == SG_BF16, mma_m, pl.bn, true);
     prm.idesc_half = esz == 1 ? sg::idesc_e4m3(mma_m, pl.bn / 2, true)
@@ -807,7 +829,7 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
 static int config_choice(const sg_config* cfg, Choice* c, int* stages) {
     const sg_config z = {};
     const sg_config& g = cfg ? *cfg : z;
-    if (g.block_n != 0 && !valid_bn(g.block_n)) return SG_ERR_CONFIG;
+    if (g.block_n != 0 && !valid_tile(g.block_n)) return SG_ERR_CONFIG;
     if (g.mode != 0 && !valid_mode(g.mode)) return SG_ERR_CONFIG;
     if (g.group_m < 0 || g.group_m > 64 || g.tail_split < -1 || g.tail_split > 1) return SG_ERR_CONFIG;
     if (g.stages < 0 || g.stages > SG_MAX_STAGES) return SG_ERR_STAGES;
@@ -900,6 +922,16 @@ int sg_tune(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const v
             Choice c;
             c.bn = 128;
             c.mode = 4;
+            cands.push_back(c);
+        }
+    }
+    if (a_tma && b_tma && m_blocks >= 2 && N > 256) {  // wide paired tiles (two 256-column accumulators)
+        for (int g : {8, 12, 16}) {
+            Choice c;
+            c.bn = 512;
+            c.mode = 6;
+            c.group_m = g;
+            if (g != 12 && m_blocks * cdiv(N, 512) <= st->sm_count) continue;
             cands.push_back(c);
         }
     }

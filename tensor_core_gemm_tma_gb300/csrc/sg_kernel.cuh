@@ -26,7 +26,7 @@
 //               TMA store that does not write elements outside M x N
 //               (gizml:tile, "Out.put").
 //
-// Four modes (MODE; the numbers are those of sg_plan_info.mode):
+// Five modes (MODE; the numbers are those of sg_plan_info.mode):
 //   1  one CTA per 128 x BN tile.
 //   4  resident B ("decoded panels", Tolk.Stage): for a small K x N, each
 //      CTA stages all of B once (every K chunk of every 128-column block)
@@ -34,6 +34,14 @@
 //      every column block of that row tile read the one A slot, each into
 //      its own rotating accumulator.  Tile units are (row tile, column
 //      block) in that order; the epilogue is the same as mode 1's.
+//   6  wide paired tiles: mode 3 with a 256 x 2BN tile (BN = 256) held as
+//      two BN-wide accumulators.  Each CTA stages its 128 rows of A once per
+//      K chunk for both accumulators and its half of each accumulator's B
+//      columns, so a K chunk moves 48 KiB per CTA for 128 x 512 x 64
+//      products instead of 32 KiB for 128 x 256 x 64 (a quarter fewer
+//      operand bytes per product).  The tile's second accumulator is claimed
+//      only after the first one's first MMAs are issued, so the epilogue of
+//      the previous tile drains it meanwhile.
 //   3  paired MMA (tcgen05 cta_group::2): the two CTAs of a cluster compute
 //      one 256 x BN tile.  Each CTA stages its own 128 rows of A and its own
 //      BN/2 columns of B (so a stage is 32 KiB instead of 48 KiB for
@@ -260,21 +268,23 @@ __device__ __forceinline__ void tile_coords(int tile, const Params& p, uint32_t 
     nb = r / gsize;
 }
 
-// Row block and first column of work unit `u` (modes 1-3); returns its width
-// in columns.  Only 256-column tiles of 16-bit operands are ever split: each
-// half is then a whole number of 64-column B boxes in every CTA.
-template <int CM, int BN, int ESZ>
+// Row block and first column of work unit `u` (modes 1, 3, 6; TW is the
+// tile width); returns its width in columns.  Only 256-column tiles of
+// 16-bit operands and 512-column wide tiles are ever split: each half is
+// then a whole number of 128-byte B boxes in every CTA.
+template <int CM, int TW, int ESZ>
 __device__ __forceinline__ int unit_coords(int u, const Params& p, uint32_t rank, int& mb, int& col0) {
+    constexpr bool SPLITTABLE = (TW == 256 && ESZ == 2) || TW == 512;
     int nb;
-    if (BN != 256 || ESZ != 2 || u < p.full_units) {
+    if (!SPLITTABLE || u < p.full_units) {
         tile_coords<CM>(u, p, rank, mb, nb);
-        col0 = nb * BN;
-        return BN;
+        col0 = nb * TW;
+        return TW;
     }
     const int v = u - p.full_units;
     tile_coords<CM>(p.full_units + (v >> 1), p, rank, mb, nb);
-    col0 = nb * BN + (v & 1) * (BN / 2);
-    return BN / 2;
+    col0 = nb * TW + (v & 1) * (TW / 2);
+    return TW / 2;
 }
 
 // Wait for phase `parity` of `bar`, giving up after `limit` ns or when another
@@ -525,14 +535,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     sg_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmR,
                    const Params p) {
-    static_assert(MODE == 1 || MODE == 3 || MODE == 4 || MODE == 5, "modes 1, 3, 4 and 5");
-    constexpr int CM = (MODE == 3) ? 2 : 1;  // CTAs per cluster
+    static_assert(MODE == 1 || MODE == 3 || MODE == 4 || MODE == 5 || MODE == 6, "modes 1, 3, 4, 5 and 6");
     constexpr bool PANEL = (MODE == 4 || MODE == 5);      // B resident in shared memory
     constexpr bool DECODE = (MODE == 5);                  // ... decoded there from int8 codes
     static_assert(!DECODE || (ESZ == 2 && !RES), "mode 5: 16-bit A, no residual");
-    constexpr bool PAIR = (MODE == 3);         // paired MMA (cta_group::2)
-    constexpr int CG = PAIR ? 2 : 1;           // cta_group of every tcgen05 instruction
-    constexpr int BL = PAIR ? BN / 2 : BN;     // B columns staged by this CTA
+    constexpr bool WIDE = (MODE == 6);                    // two BN-wide accumulators per paired tile
+    static_assert(!WIDE || BN == 256, "wide tiles hold two 256-column accumulators");
+    constexpr bool PAIR = (MODE == 3 || WIDE);  // paired MMA (cta_group::2)
+    constexpr int CM = PAIR ? 2 : 1;            // CTAs per cluster
+    constexpr int NSUB = WIDE ? 2 : 1;          // accumulators per tile
+    constexpr int TW = BN * NSUB;               // tile width in columns
+    constexpr int CG = PAIR ? 2 : 1;            // cta_group of every tcgen05 instruction
+    constexpr int BL = PAIR ? TW / 2 : BN;      // B columns staged by this CTA
     using L = Layout<BN, BL>;
     using G = Geom<ESZ>;
     static_assert(BL % G::BOXC == 0, "B is staged in whole 128-byte-wide boxes");
@@ -688,13 +702,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             for (int tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 int mb = tile, col0 = 0, width = BN;
-                if constexpr (!PANEL) width = unit_coords<CM, BN, ESZ>(tile, p, rank, mb, col0);
+                if constexpr (!PANEL) width = unit_coords<CM, TW, ESZ>(tile, p, rank, mb, col0);
                 // B columns landing in this CTA per K chunk: the paired MMA stages
                 // half of the unit's columns in each CTA
                 const int bl = PAIR ? width / 2 : width;
                 const uint32_t chunk_tx = A_STAGE_BYTES + static_cast<uint32_t>(bl) * BK_BYTES;
                 const int fills = PANEL ? 1 : p.k_chunks;  // mode 4: one ring slot holds every K chunk of A
                 const int grp = PANEL ? 1 : ring_group;
+                // paired: each accumulator's columns (sw of them) are split
+                // between the two CTAs, this CTA staging [rank * sw / 2, +sw / 2)
+                // of each in bps boxes
+                const int sw = WIDE ? BN : width;
+                const int bps = (sw / 2) / G::BOXC;
                 for (int kc = 0; kc < fills; kc += grp, it += grp) {
                     if (!wait_bounded(empty_bar(slot), phase ^ 1u, abort_flag, p.status, p.wait_limit_ns,
                                       SITE_PRODUCER_EMPTY)) {
@@ -718,7 +737,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 tma_load_2d_pair(sc, &tmA, fb, k0, mb * BM);
                                 for (int j = 0; j < bl / G::BOXC; ++j)
                                     tma_load_2d_pair(sc + A_STAGE_BYTES + j * G::B_BOX_BYTES, &tmB, fb,
-                                                     col0 + static_cast<int>(rank) * bl + j * G::BOXC, k0);
+                                                     col0 + (j / bps) * sw + static_cast<int>(rank) * (sw / 2) +
+                                                         (j % bps) * G::BOXC,
+                                                     k0);
                             }
                         } else {
                             mbar_arrive_expect_tx(full_bar(slot), nq * chunk_tx);
@@ -810,14 +831,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     continue;
                 }
-                if (!wait_all(tempty_bar(ab), aph ^ 1u, SITE_MMA_TMEM_EMPTY)) {
+                int umb, ucol;
+                const int uw = unit_coords<CM, TW, ESZ>(tile, p, rank, umb, ucol);
+                const int nsub = WIDE ? uw / BN : 1;  // accumulators this unit fills
+                const uint32_t idesc = (WIDE || uw == BN) ? p.idesc : p.idesc_half;
+                // the unit's accumulators in rotation order; the first is claimed
+                // now, the others just before their first MMA
+                uint32_t sab[NSUB] = {}, saph[NSUB] = {};
+#pragma unroll
+                for (int h = 0; h < NSUB; ++h) {
+                    if (h < nsub) {
+                        sab[h] = ab;
+                        saph[h] = aph;
+                        if (++ab == static_cast<uint32_t>(ACC)) {
+                            ab = 0;
+                            aph ^= 1u;
+                        }
+                    }
+                }
+                if (!wait_all(tempty_bar(sab[0]), saph[0] ^ 1u, SITE_MMA_TMEM_EMPTY)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + ab * BN;
-                int umb, ucol;
-                const uint32_t idesc = unit_coords<CM, BN, ESZ>(tile, p, rank, umb, ucol) == BN ? p.idesc : p.idesc_half;
                 // Slots come in groups of ring_group on one full and one empty
                 // barrier: each wait stalls this warp long enough for the tensor
                 // pipe to run dry, so fewer waits per MMA keep it busier.
@@ -827,33 +863,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    if (issuer) {
-                        const int nq = min(ring_group, p.k_chunks - kc);
-                        for (int c = 0; c < nq; ++c) {
-                            const int kk = kc + c;
-                            const uint32_t sa = ring0 + (slot + c) * stage_bytes;
-                            // A: K-major, 8-row groups 1024 B apart.  B: MN-major, 8-K-row
-                            // groups 1024 B apart, 64-column blocks one TMA box apart.
-                            const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
-                            const uint64_t b_desc = smem_desc_sw128(sa + A_STAGE_BYTES, G::B_BOX_BYTES, 1024);
-                            // K steps that lie wholly past K would only add products of
-                            // zero-filled elements: skip them
-                            const int ksteps = min(G::KB / G::UK, (p.K - kk * G::KB + G::UK - 1) / G::UK);
+                    const int nq = min(ring_group, p.k_chunks - kc);
 #pragma unroll
-                            for (int k = 0; k < G::KB / G::UK; ++k) {
-                                // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
-                                if (k < ksteps) {
-                                    const uint64_t ad = a_desc + ((k * 32) >> 4);  // +32 bytes of K along the row
-                                    const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
-                                    const uint32_t acc = (kk | k) != 0 ? 1u : 0u;
-                                    if constexpr (PAIR) {
-                                        umma_pair<ESZ>(d_tmem, ad, bd, idesc, acc);
-                                    } else {
-                                        umma<ESZ>(d_tmem, ad, bd, idesc, acc);
+                    for (int h = 0; h < NSUB; ++h) {
+                        if (h >= nsub) break;
+                        if (h > 0 && kc == 0) {
+                            // a wide tile's next accumulator, claimed only now: the
+                            // previous tile's epilogue drains it while the first
+                            // accumulator's first MMAs run
+                            if (!wait_all(tempty_bar(sab[h]), saph[h] ^ 1u, SITE_MMA_TMEM_EMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        if (issuer) {
+                            const uint32_t d_tmem = tmem_base + sab[h] * BN;
+                            for (int c = 0; c < nq; ++c) {
+                                const int kk = kc + c;
+                                const uint32_t sa = ring0 + (slot + c) * stage_bytes;
+                                // A: K-major, 8-row groups 1024 B apart.  B: MN-major, 8-K-row
+                                // groups 1024 B apart, 64-column blocks one TMA box apart; a
+                                // wide tile's second accumulator reads the boxes after the first's.
+                                const uint64_t a_desc = smem_desc_sw128(sa, 16, 1024);
+                                const uint64_t b_desc = smem_desc_sw128(
+                                    sa + A_STAGE_BYTES + h * ((BN / 2) / G::BOXC) * G::B_BOX_BYTES, G::B_BOX_BYTES,
+                                    1024);
+                                // K steps that lie wholly past K would only add products of
+                                // zero-filled elements: skip them
+                                const int ksteps = min(G::KB / G::UK, (p.K - kk * G::KB + G::UK - 1) / G::UK);
+#pragma unroll
+                                for (int k = 0; k < G::KB / G::UK; ++k) {
+                                    // K step of 16: +32 bytes along A's swizzled row, +2 groups of 8 rows of B
+                                    if (k < ksteps) {
+                                        const uint64_t ad = a_desc + ((k * 32) >> 4);  // +32 bytes of K along the row
+                                        const uint64_t bd = b_desc + ((k * G::B_KSTEP_BYTES) >> 4);
+                                        const uint32_t acc = (kk | k) != 0 ? 1u : 0u;
+                                        if constexpr (PAIR) {
+                                            umma_pair<ESZ>(d_tmem, ad, bd, idesc, acc);
+                                        } else {
+                                            umma<ESZ>(d_tmem, ad, bd, idesc, acc);
+                                        }
                                     }
                                 }
                             }
                         }
+                    }
+                    if (!ok) break;
+                    if (issuer) {
                         if constexpr (PAIR) {
                             umma_commit_pair_multicast(empty_bar(slot), CLUSTER_MASK);  // frees the slots in both CTAs
                         } else {
@@ -868,15 +925,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 if (issuer) {
-                    if constexpr (PAIR) {
-                        umma_commit_pair_multicast(tfull_bar(ab), CLUSTER_MASK);  // both CTAs' epilogues
-                    } else {
-                        umma_commit(tfull_bar(ab));
+#pragma unroll
+                    for (int h = 0; h < NSUB; ++h) {
+                        if (h < nsub) {
+                            if constexpr (PAIR) {
+                                umma_commit_pair_multicast(tfull_bar(sab[h]), CLUSTER_MASK);  // both CTAs' epilogues
+                            } else {
+                                umma_commit(tfull_bar(sab[h]));
+                            }
+                        }
                     }
-                }
-                if (++ab == static_cast<uint32_t>(ACC)) {
-                    ab = 0;
-                    aph ^= 1u;
                 }
             }
             // every MMA of this CTA has completed before tensor memory is released
@@ -927,11 +985,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32) : "memory");
         }
         uint32_t ab = 0, aph = 0;
-        // units: one per tile (modes 1-3), or (row tile, column block) pairs (modes 4, 5)
-        const int subs = PANEL ? p.n_blocks : 1;
+        // accumulators: one per unit (modes 1, 3), one per column block of a row
+        // tile (modes 4, 5), one per BN columns of a unit (mode 6)
+        int subs = PANEL ? p.n_blocks : 1;
         for (int tile = cluster_id, sub = 0; tile < p.num_tiles;) {
             int mb = tile, ucol = sub * BN, width = BN;
-            if constexpr (!PANEL) width = unit_coords<CM, BN, ESZ>(tile, p, rank, mb, ucol);
+            if constexpr (WIDE) {
+                int u0;
+                subs = unit_coords<CM, TW, ESZ>(tile, p, rank, mb, u0) / BN;
+                ucol = u0 + sub * BN;
+            } else if constexpr (!PANEL) {
+                width = unit_coords<CM, TW, ESZ>(tile, p, rank, mb, ucol);
+            }
             const int row0 = mb * BM + q * 32;
             const int row = row0 + lane;
             // the residual of this warp's first chunk loads while the MMAs run

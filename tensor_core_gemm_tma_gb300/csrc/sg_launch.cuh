@@ -35,7 +35,7 @@ using LaunchFn = int (*)(LaunchArgs&);
 
 template <int BN, int OUT, int MODE, bool RES, int ESZ>
 int launch_kernel(LaunchArgs& a) {
-    constexpr int CM = (MODE == 3) ? 2 : 1;  // CTAs per cluster
+    constexpr int CM = (MODE == 3 || MODE == 6) ? 2 : 1;  // CTAs per cluster
     auto kern = sg_gemm_kernel<BN, OUT, MODE, RES, ESZ>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -88,5 +88,7 @@ LaunchFn launcher_fp8_res(int bn, int out, int mode);
 // Mode 4 (resident B), tile width 128, either element size (esz 1 or 2):
 LaunchFn launcher_panel(int out, bool residual, int esz);
 LaunchFn launcher_decoded(int out);  // mode 5: 16-bit A, int8-coded B decoded into the resident panel
+// Mode 6 (wide paired tiles: two 256-column accumulators), either element size:
+LaunchFn launcher_wide(int out, bool residual, int esz);
 
 }  // namespace sg

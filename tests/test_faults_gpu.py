@@ -12,7 +12,7 @@ from parity_util import compare, run_gpu, seeded_case
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", [1, 3])
+@pytest.mark.parametrize("mode", [1, 3, 6])
 def test_skipped_copy_times_out_and_context_survives(mode):
     import torch
     from tensor_core_gemm_tma_gb300 import _build
@@ -28,7 +28,8 @@ def test_skipped_copy_times_out_and_context_survives(mode):
         assert lib.sg_test_set_cluster(mode) == 0
         assert lib.sg_test_set_tile_n(256) == 0
         p = sg.plan(M, N, K, torch.float16, torch.float32)
-        assert p["cluster_m"] == (1 if mode == 1 else 2) and p["pair_mma"] == (1 if mode == 3 else 0)
+        assert p["cluster_m"] == (1 if mode == 1 else 2) and p["pair_mma"] == (0 if mode == 1 else 1)
+        assert p["mode"] == mode
         sg.set_wait_limit_ns(50_000_000)          # 50 ms
         lib.sg_test_set_skip_load(1)
         sg.stage_gemm(A, B)                       # the launch itself succeeds

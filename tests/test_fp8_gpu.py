@@ -98,3 +98,34 @@ def test_fp8_square8192_sampled():
     cols = np.concatenate([rng.integers(0, w.N, 4096), np.arange(w.N), np.full(w.M, w.N - 1)])
     ref, _, S = oracle.gemm_at(a, b, rows, cols, "e4m3", "bf16")
     compare(got[rows, cols], ref, S, "bf16", "square8192_e4m3")
+
+
+def test_fp8_wide_tiles_bit_identical():
+    """FP8 operands in 256 x 512 paired tiles of two accumulators (mode 6; a
+    B box is 128 FP8 columns, so each CTA stages one box per accumulator):
+    the bits of the 256 x 256 paired tiles and of single CTAs, at every
+    depth, with a split tail."""
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    from parity_util import from_device_bits, to_device_bits
+    M, N, K = 2500, 4700, 640
+    a, b = _case(M, N, K, seed=103)
+    dev = torch.device("cuda")
+    A = to_device_bits(a, "e4m3", dev)
+    B = to_device_bits(b, "e4m3", dev)
+    assert sg.plan(M, N, K, torch.float8_e4m3fn, torch.bfloat16, config={"block_n": 512})["tail_units"] > 0
+
+    def run(cfg):
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        sg.stage_gemm(A, B, out=C, config=cfg)
+        assert sg.device_status() == 0
+        return from_device_bits(C, "bf16")
+    ref = run({"block_n": 256, "mode": 3})
+    assert np.array_equal(run({"block_n": 256, "mode": 1}), ref)
+    for s in (1, 2, 4):
+        assert np.array_equal(run({"block_n": 512, "mode": 6, "stages": s}), ref), s
+    rng = np.random.default_rng(7)
+    rows = np.concatenate([rng.integers(0, M, 3000), np.full(N, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, 3000), np.arange(N)])
+    r, _, S = oracle.gemm_at(a, b, rows, cols, "e4m3", "bf16")
+    compare(ref[rows, cols], r, S, "bf16", "fp8 wide")

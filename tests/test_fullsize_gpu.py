@@ -166,7 +166,8 @@ def test_config_rejects_what_the_problem_cannot_take():
     import tensor_core_gemm_tma_gb300 as sg
     A = torch.zeros((512, 512), dtype=torch.float16, device="cuda")
     B = torch.zeros((512, 512), dtype=torch.float16, device="cuda")
-    for cfg in ({"block_n": 192, "mode": 3}, {"mode": 4}, {"block_n": 256, "mode": 4}):
+    for cfg in ({"block_n": 192, "mode": 3}, {"mode": 4}, {"block_n": 256, "mode": 4}, {"block_n": 256, "mode": 6},
+                {"block_n": 512, "mode": 3}, {"block_n": 512, "mode": 1}):
         with pytest.raises(sg.SgError) as e:
             sg.stage_gemm(A, B, config=cfg)
         assert e.value.code == -9, cfg
@@ -180,3 +181,21 @@ def test_config_rejects_what_the_problem_cannot_take():
         assert e.value.code == -9, cfg
     torch.cuda.synchronize()
     assert sg.device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["square8192_bf16", "square8192_e4m3", "relu4096_f16"])
+def test_wide_tiles_full_size_bit_identical(name):
+    """256 x 512 paired tiles of two accumulators (mode 6) at the workloads'
+    full sizes, at the deepest ring and at 2 slots: the bits of the
+    planner's configuration."""
+    import torch
+    w = gemm_inputs.WORKLOADS[name]
+    host_ops, dev_ops = _operands(w)
+    ref = _run(w, dev_ops)
+    assert _plan(w, config={"block_n": 512})["mode"] == 6
+    for s in (0, 2):
+        assert torch.equal(_run(w, dev_ops, config={"block_n": 512, "mode": 6, "stages": s}), ref), f"stages={s}"
+    if name == "square8192_bf16":
+        edge = (0,) + tuple(range(w.M - 256, w.M))
+        rows, cols = _sample(w, 4096, edge_rows=edge, edge_cols=edge)
+        _sampled_check(w, host_ops, ref, rows, cols, name)

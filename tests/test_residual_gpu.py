@@ -146,3 +146,32 @@ def test_backproj_workload_sampled():
     rr = decode_np(ref, "f16")
     tol = oracle.tolerance(S, rr, "f16", added=np.abs(decode_np(r[rows, cols], "f16")))
     assert np.all(np.abs(g - rr) <= tol)
+
+
+@pytest.mark.parametrize("out_dt", ["f16", "f32"])
+def test_residual_wide_tiles_bit_identical(out_dt):
+    """The residual through every paired form: 256 x 256 tiles (mode 3) and
+    256 x 512 tiles of two accumulators (mode 6), in place and not, give the
+    single-CTA bits."""
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    from parity_util import torch_dtype
+    M, N, K = 1130, 1300, 520
+    a, b = seeded_case(M, N, K, "f16", seed=61)
+    r = _rbits(M, N, out_dt, seed=62)
+    dev = torch.device("cuda")
+    A = to_device_bits(a, "f16", dev)
+    B = to_device_bits(b, "f16", dev)
+    outs = {}
+    for name, cfg in (("single", {"block_n": 256, "mode": 1}), ("pair", {"block_n": 256, "mode": 3}),
+                      ("wide", {"block_n": 512, "mode": 6})):
+        R = to_device_bits(r, out_dt, dev)
+        C = torch.empty((M, N), dtype=torch_dtype(out_dt), device=dev)
+        sg.stage_gemm(A, B, epilogue="relu", out=C, residual=R, config=cfg)
+        outs[name] = from_device_bits(C, out_dt)
+        sg.stage_gemm(A, B, epilogue="relu", out=R, residual=R, config=cfg)   # in place
+        outs[name + " in place"] = from_device_bits(R, out_dt)
+        assert sg.device_status() == 0
+    for k, o in outs.items():
+        assert np.array_equal(o, outs["single"]), k
+    check(outs["wide"], a, b, r, "f16", out_dt, "relu", what="residual wide")

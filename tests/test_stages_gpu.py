@@ -226,3 +226,60 @@ def test_paired_slots_only_with_tma_operands():
         lib.sg_test_set_tile_n(0)
     ref, _, S = oracle.gemm(a, b, "f16", "f32", K=K)
     compare(out, ref, S, "f32", "element loads, 6 slots")
+
+
+def _cfg_run(a, b, M, N, K, ind, outd, epi, cfg, bias=None):
+    """run_gpu through sg_gemm_ex under the configuration `cfg`."""
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    from parity_util import from_device_bits, to_device_bits, torch_dtype
+    dev = torch.device("cuda")
+    A = to_device_bits(a, ind, dev)[:, :K]
+    B = to_device_bits(b, ind, dev)[:, :N]
+    C = torch.empty((M, N), dtype=torch_dtype(outd), device=dev)
+    bias_d = None if bias is None else torch.from_numpy(np.ascontiguousarray(bias, np.float32)).to(dev)
+    sg.stage_gemm(A, B, epilogue=epi, bias=bias_d, out=C, config=cfg)
+    assert sg.device_status() == 0
+    return from_device_bits(C, outd)
+
+
+WIDE_CASES = [
+    # M, N, K, in, out, epilogue: odd row blocks, N ragged inside a tile's second accumulator, ragged K
+    (1130, 1300, 9 * 64 - 3, "bf16", "bf16", "none"),
+    (1130, 1300, 9 * 64 - 3, "f16", "f32", "relu"),
+    # 10 x 10 wide tiles over 76 clusters: the last 24 run as 48 half units (one accumulator each)
+    (2500, 4700, 300, "f16", "f16", "bias_relu"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,ind,outd,epi", WIDE_CASES)
+def test_wide_tiles_bit_identical(M, N, K, ind, outd, epi):
+    """Mode 6 (a CTA pair computes a 256 x 512 tile as two 256-column
+    accumulators, each CTA staging A once for both) issues, for every output
+    element, the same MMAs in the same K order as the paired 256 x 256 tiles
+    (mode 3) and the single-CTA tiles (mode 1): C must be bit-identical at
+    every ring depth, with the split tail on and off."""
+    a, b = seeded_case(M, N, K, ind, seed=51, lda=(K + 7) // 8 * 8)
+    bias = np.linspace(-2, 2, N).astype(np.float32) if epi == "bias_relu" else None
+    p = _plan(M, N, K, ind, outd)
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    t = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    pw = sg.plan(M, N, K, t[ind], t[outd], epi, config={"block_n": 512, "mode": 6})
+    assert pw["mode"] == 6 and pw["block_n"] == 512 and pw["pair_mma"] == 1 and pw["cluster_m"] == 2
+    assert pw["max_stages"] == 4 and pw["ring_group"] == 1
+    if M == 2500:
+        assert pw["tail_units"] > 0
+    ref = _cfg_run(a, b, M, N, K, ind, outd, epi, {"block_n": 256, "mode": 3}, bias)
+    assert np.array_equal(_cfg_run(a, b, M, N, K, ind, outd, epi, {"block_n": 256, "mode": 1}, bias), ref)
+    for s in (1, 2, 3, 4):
+        got = _cfg_run(a, b, M, N, K, ind, outd, epi, {"block_n": 512, "mode": 6, "stages": s}, bias)
+        assert np.array_equal(got, ref), f"mode 6, stages={s}"
+    got = _cfg_run(a, b, M, N, K, ind, outd, epi, {"block_n": 512, "tail_split": -1}, bias)
+    assert np.array_equal(got, ref), "mode 6 without the split tail"
+    rng = np.random.default_rng(M)
+    rows = np.concatenate([rng.integers(0, M, 3000), np.full(N, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, 3000), np.arange(N)])
+    r, _, S = oracle.gemm_at(a, b, rows, cols, ind, outd, epi, bias, K=K)
+    compare(ref[rows, cols], r, S, outd, f"wide tiles {ind}->{outd} {epi}")
+    assert p["block_m"] == 128
