@@ -108,7 +108,7 @@ def test_fp8_wide_tiles_bit_identical():
     import torch
     import tensor_core_gemm_tma_gb300 as sg
     from parity_util import from_device_bits, to_device_bits
-    M, N, K = 2500, 4700, 640
+    M, N, K = 2500, 4736, 640                     # FP8 rows of 4736 bytes: TMA-legal
     a, b = _case(M, N, K, seed=103)
     dev = torch.device("cuda")
     A = to_device_bits(a, "e4m3", dev)

@@ -244,11 +244,13 @@ def _cfg_run(a, b, M, N, K, ind, outd, epi, cfg, bias=None):
 
 
 WIDE_CASES = [
-    # M, N, K, in, out, epilogue: odd row blocks, N ragged inside a tile's second accumulator, ragged K
-    (1130, 1300, 9 * 64 - 3, "bf16", "bf16", "none"),
-    (1130, 1300, 9 * 64 - 3, "f16", "f32", "relu"),
-    # 10 x 10 wide tiles over 76 clusters: the last 24 run as 48 half units (one accumulator each)
-    (2500, 4700, 300, "f16", "f16", "bias_relu"),
+    # M, N, K, in, out, epilogue (B pitches TMA-legal: the paired forms need TMA operands): odd row
+    # blocks, N ragged inside a tile's second accumulator, ragged K
+    (1130, 1304, 9 * 64 - 3, "bf16", "bf16", "none"),
+    (1130, 1304, 9 * 64 - 3, "f16", "f32", "relu"),
+    # 10 x 10 wide tiles over 76 clusters (the last column block 96 wide: its second accumulator wholly
+    # past N); the last 24 tiles run as 48 half units (one accumulator each)
+    (2500, 4704, 300, "f16", "f16", "bias_relu"),
 ]
 
 
