@@ -685,7 +685,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0 && p.k_chunks > 0) {
+        // one elected thread issues every copy
+        if (elect_one_sync() && p.k_chunks > 0) {
             uint32_t slot = 0, phase = 0;
             uint32_t issued = 0, last_parity = 0;  // per slot: ever filled, parity of its last fill
             int64_t it = 0;
@@ -773,9 +774,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         // The whole warp runs the loop, so slots, phases and descriptors stay
-        // warp-uniform; lane 0 issues each tcgen05 instruction.
+        // warp-uniform; one elected lane (lane 0) issues each tcgen05
+        // instruction.
         if (p.k_chunks > 0 && (!PAIR || rank == 0)) {
-            const bool issuer = lane == 0;
+            const bool issuer = elect_one_sync();
             auto wait_all = [&](uint32_t bar, uint32_t parity, int site) {
                 return __all_sync(0xffffffffu, wait_fast(bar, parity, abort_flag, p.status, p.wait_limit_ns, site));
             };
@@ -954,13 +956,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr int SPLIT = EPI_WARPS / 4;      // warps sharing a quarter
         const int part = e / 4;                   // which of them: takes column chunks part, part+SPLIT, ...
         const uint32_t buf = base + epi_off + e * EPI_BUF_BYTES;
+        // the lane that issues this warp's TMA copies and waits for them
+        // (bulk groups belong to the thread that committed them)
+        const bool leader = elect_one_sync();
         const bool r_staged = RES && p.r_tma;  // residual tiles arrive by TMA in the staging buffer
         uint32_t r_phase = 0;
         bool r_pending = false;                    // a residual load is in flight into `buf`
         // Starts the TMA load of the residual box this warp needs for output
         // columns col0.. (after the previous store has read the buffer).
         auto load_residual = [&](int row0, int col0) {
-            if (lane == 0) {
+            if (leader) {
                 bulk_wait_group_read<0>();
                 mbar_arrive_expect_tx(rres_bar(e), EPI_BUF_BYTES);
                 tma_load_2d(buf, &tmR, rres_bar(e), col0, row0);
@@ -972,7 +977,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             decode_panel(base, p, p.n_blocks, p.k_chunks, B_BLOCK_BYTES, G::B_BOX_BYTES, e, EPI_WARPS, lane);
             fence_proxy_async_smem();  // the MMA reads it through the async proxy
             __syncwarp();
-            if (lane == 0) mbar_arrive(bres_bar);
+            if (leader) mbar_arrive(bres_bar);
             // the per-column scales and biases, read by every chunk of every tile
             const bool has_bias = p.epi == SG_EPI_BIAS_RELU;
             for (int i = e * 32 + lane; i < p.n_blocks * BN; i += EPI_WARPS * 32) {
@@ -1064,7 +1069,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (p.tma_store) {
                     if (row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
                         // the previous store has read the buffer (a staged residual already waited)
-                        if (lane == 0 && !r_staged) bulk_wait_group_read<0>();
+                        if (leader && !r_staged) bulk_wait_group_read<0>();
                         __syncwarp();
                         const uint32_t rowaddr = buf + lane * 128;
 #pragma unroll
@@ -1091,7 +1096,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) {
+                        if (leader) {
                             tma_store_2d(&tmC, buf, col0, row0);
                             bulk_commit_group();
                         }
@@ -1111,7 +1116,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (p.k_chunks > 0) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
+                if (leader) {
                     if constexpr (PAIR) {
                         mbar_arrive_cluster(mapa_shared(tempty_bar(ab), 0));  // the even CTA's MMA waits on it
                     } else {
@@ -1129,8 +1134,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         // leaving early with a residual load in flight: let it land first
-        if (r_pending && lane == 0) wait_drain(rres_bar(e), r_phase, p.wait_limit_ns);
-        if (lane == 0) bulk_wait_group<0>();
+        if (r_pending && leader) wait_drain(rres_bar(e), r_phase, p.wait_limit_ns);
+        if (leader) bulk_wait_group<0>();
         __syncwarp();
     }
 
