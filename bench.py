@@ -354,6 +354,7 @@ def config_of(w, plan, flush_mode="write+read"):
         c["stages"] = plan["stages"]
         c["grid"] = plan["grid"]
         c["kernel_mode"] = {1: "single CTA", 3: "paired MMA (cta_group::2)",
+                            6: "paired MMA over 256x512 tiles, two 256-column accumulators (cta_group::2)",
                             4: "resident B (one CTA per row tile, all of B in shared memory)",
                             5: "decoded panel (int8-coded B decoded once per CTA into the resident shared-memory "
                                "panel)"}.get(plan.get("mode"))

@@ -317,9 +317,19 @@ std::atomic<int> g_force_mode{[] {
     return valid_mode(x) ? x : 0;
 }()};
 
+// Waves of `units` work units over `slots` clusters, the last wave counted
+// half when it would be split into half-width units (fills at most half of
+// the slots; see the tail split below).
+double wave_count(int64_t units, int64_t slots, bool splittable) {
+    const int64_t full = units / slots, tail = units % slots;
+    double w = static_cast<double>(full);
+    if (tail) w += (splittable && full > 0 && 2 * tail <= slots) ? 0.5 : 1.0;
+    return w;
+}
+
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, const void* C,
               int64_t ldc, int stages, bool a_tma, bool b_tma, Plan* pl, const Choice* choice = nullptr,
-              bool decode = false) {
+              bool decode = false, bool residual = false) {
     const int esz = elem_bytes(in_dtype);
     const int boxc = 128 / esz;  // B columns per 128-byte box: tile widths and CTA shares are multiples
     pl->a_tma = a_tma ? 1 : 0;
@@ -372,6 +382,24 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // its half of B.  A pair tile is two SMs' work, so pairing keeps as many
     // SMs busy as single-CTA tiles do.
     int mode = (pl->k_chunks >= 8 && pl->m_blocks >= 2 && pairable) ? 3 : 1;
+    // Mode 6 (a CTA pair computes 256 x 512 as two 256-column accumulators:
+    // a quarter fewer operand bytes per product and half as many tiles)
+    // instead of paired 256-column tiles when its waves cost less, counting
+    // its per-SM throughput at full load as 1.08 of theirs (measured on
+    // GB300: 8192^3 bf16 +7.9%, FP8 +3.9%, 16384 x 8192 x 4096 +3.3%,
+    // 6144 x 12288 x 4096 +1.4%, 8192^2 x 2048 +1.3%; 4096^3 -2% and 2048^3
+    // -29%, both rejected by the wave count).  Only with a long K loop (the
+    // tile boundary, where the second accumulator waits for the previous
+    // tile's epilogue to read it, then weighs little), a 16-bit output and no
+    // residual (there the epilogue hands the accumulator back before storing).
+    bool auto_wide = false;
+    if (mode == 3 && bn == 256 && !bn_forced && pl->k_chunks >= 32 && out_dtype != SG_F32 && !residual && a_tma &&
+        b_tma && !decode) {
+        const int64_t clusters = st.sm_count / 2, mc = cdiv(pl->m_blocks, 2);
+        const double c3 = wave_count(mc * cdiv(N, 256), clusters, esz == 2) * 256.0;
+        const double c6 = wave_count(mc * cdiv(N, 512), clusters, true) * 512.0 / 1.08;
+        auto_wide = c6 < 0.98 * c3;
+    }
     // Mode 4 (resident B) when B is small: at most 2 K chunks and 4 column
     // blocks of 128, so all of B fits next to a ring of at least 2 A tiles,
     // and there are enough row tiles to keep every SM busy.
@@ -382,6 +410,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     auto legal = [&](int m) {
         return m == 1 || (m == 3 && pairable) || (m == 4 && panel_ok) || (m == 6 && bn == 256 && a_tma && b_tma);
     };
+    if (auto_wide && legal(6)) mode = 6;
     if (const int f = g_force_mode.load(); f && legal(f)) mode = f;
     if (choice && choice->mode && legal(choice->mode)) mode = choice->mode;
     if (wide && legal(6)) mode = 6;
@@ -584,7 +613,7 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
         lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, a_tma, b_tma, c_tma_legal(C, M, ldc, out_dtype), &tuned))
         choice = &tuned;
     Plan pl;
-    int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice, decode);
+    int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice, decode, R != nullptr);
     if (rc != SG_OK) return rc;
     if (choice && choice->strict && !honours(pl, *choice)) return SG_ERR_CONFIG;
     if (used) *used = pl;

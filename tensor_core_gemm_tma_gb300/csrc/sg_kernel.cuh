@@ -1014,6 +1014,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
             }
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN;
+            // Mode 6, 16-bit output, no residual: this warp's columns of the
+            // accumulator are read into registers (converted and packed) and
+            // the accumulator handed back before any of them is stored.  The
+            // next tile's MMAs need this accumulator after a few of their first
+            // MMAs, so the tile boundary waits only for the reads.
+            constexpr bool EARLY = WIDE && OUT != SG_F32 && !RES;
+            if (EARLY && p.k_chunks > 0 && p.tma_store) {
+                constexpr int NCH = BN / (SPLIT * COLS);  // this warp's 64-column chunks
+                uint32_t pk[NCH][COLS / 2];
+                const bool relu = p.epi != SG_EPI_NONE;
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) {
+                    const int c = part * COLS + i * SPLIT * COLS;
+                    uint32_t r[32], r2[32];
+                    tmem_ld_32x32b_x32(t_row + c, r);
+                    tmem_ld_32x32b_x32(t_row + c + 32, r2);
+                    tmem_wait_ld_dep(r);
+                    tmem_wait_ld_dep(r2);  // already complete; orders the uses of r2
+                    float v[COLS];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        v[j] = __uint_as_float(r[j]);
+                        v[32 + j] = __uint_as_float(r2[j]);
+                    }
+                    if (p.epi == SG_EPI_BIAS_RELU) add_bias<COLS>(v, p.bias, ucol + c, p.N);
+#pragma unroll
+                    for (int j = 0; j < COLS / 2; ++j)
+                        pk[i][j] = relu ? pack2_relu<OUT>(v[2 * j], v[2 * j + 1]) : pack2<OUT>(v[2 * j], v[2 * j + 1]);
+                }
+                // every value this warp needs is in registers: hand the accumulator back
+                tc_fence_before();
+                __syncwarp();
+                if (leader) {
+                    if constexpr (PAIR) {
+                        mbar_arrive_cluster(mapa_shared(tempty_bar(ab), 0));
+                    } else {
+                        mbar_arrive(tempty_bar(ab));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) {
+                    const int col0 = ucol + part * COLS + i * SPLIT * COLS;
+                    if (row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
+                        if (leader) bulk_wait_group_read<0>();  // the previous store has read the buffer
+                        __syncwarp();
+                        const uint32_t rowaddr = buf + lane * 128;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), pk[i][4 * j], pk[i][4 * j + 1],
+                                         pk[i][4 * j + 2], pk[i][4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (leader) {
+                            tma_store_2d(&tmC, buf, col0, row0);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+                __syncwarp();
+                if (++ab == static_cast<uint32_t>(ACC)) {
+                    ab = 0;
+                    aph ^= 1u;
+                }
+                if (++sub == subs) {
+                    sub = 0;
+                    tile += num_clusters;
+                }
+                continue;
+            }
 #pragma unroll 1
             for (int c = part * COLS; c < width; c += SPLIT * COLS) {
                 const int col0 = ucol + c;

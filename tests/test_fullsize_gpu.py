@@ -2,11 +2,12 @@
 
 * Staging moves values and never rounds them (Tolk.Stage, module overview),
   so the ring depth cannot change C: the 8192^3 bf16 product in the
-  benchmark's launch shape (paired 256 x 256 tiles, 6 slots on 3 barrier
-  pairs, a split last wave, 13.5 waves of tiles per CTA pair) must give the
-  same bits at 1, 2 and 4 slots; so must the skinny-K projection's resident-B
-  kernel at 1, 2 and 3 slots, and the 4096^3 ReLU product.  Many wraps of the
-  ring over many tiles per CTA are exactly where a slot race would show.
+  benchmark's launch shape (paired 256 x 512 tiles of two accumulators, 4
+  slots, 6.7 waves) and in the paired 256 x 256 form (6 slots on 3 barrier
+  pairs, a split last wave, 13.5 waves) must give the same bits at every
+  depth; so must the skinny-K projection's resident-B kernel at 1, 2 and 3
+  slots, and the 4096^3 ReLU product.  Many wraps of the ring over many
+  tiles per CTA are exactly where a slot race would show.
 * gizml:tile's fused example computes relu(A.B) over 128 x 128 output tiles,
   and "tune" says every configuration computes the same result: the 4096^3
   ReLU product with 128 x 128 tiles (one CTA per tile, or CTA pairs whose
@@ -92,13 +93,17 @@ def test_square8192_bf16_stage_counts_bit_identical():
     w = gemm_inputs.WORKLOADS["square8192_bf16"]
     host_ops, dev_ops = _operands(w)
     p = _plan(w)
-    # the benchmark's launch shape: paired 256 x 256 tiles, 6 slots in 3
-    # barrier pairs, a split last wave
-    assert p["pair_mma"] == 1 and p["block_n"] == 256 and p["stages"] == 6 and p["ring_group"] == 2
-    assert p["tail_units"] > 0
+    # the benchmark's launch shape: paired 256 x 512 tiles (mode 6), 4 slots
+    assert p["pair_mma"] == 1 and p["block_n"] == 512 and p["mode"] == 6 and p["stages"] == 4
     ref = _run(w, dev_ops, stages=0)
-    for s in (1, 2, 4):
-        assert torch.equal(_run(w, dev_ops, stages=s), ref), f"stages={s} differs from the 6-slot ring"
+    for s in (1, 2, 3):
+        assert torch.equal(_run(w, dev_ops, stages=s), ref), f"stages={s} differs from the 4-slot ring"
+    # paired 256 x 256 tiles: 6 slots in 3 barrier pairs, a split last wave
+    pair = {"block_n": 256, "mode": 3}
+    p3 = _plan(w, config=pair)
+    assert p3["stages"] == 6 and p3["ring_group"] == 2 and p3["tail_units"] > 0
+    for s in (0, 1, 2, 4):
+        assert torch.equal(_run(w, dev_ops, config=dict(pair, stages=s)), ref), f"256x256, stages={s}"
     edge = (0,) + tuple(range(w.M - 256, w.M))
     rows, cols = _sample(w, 4096, edge_rows=edge, edge_cols=edge)
     _sampled_check(w, host_ops, ref, rows, cols, "square8192_bf16, 6 slots")
@@ -186,12 +191,12 @@ def test_config_rejects_what_the_problem_cannot_take():
 @pytest.mark.parametrize("name", ["square8192_bf16", "square8192_e4m3", "relu4096_f16"])
 def test_wide_tiles_full_size_bit_identical(name):
     """256 x 512 paired tiles of two accumulators (mode 6) at the workloads'
-    full sizes, at the deepest ring and at 2 slots: the bits of the
-    planner's configuration."""
+    full sizes, at the deepest ring and at 2 slots: the bits of the paired
+    256 x 256 tiles."""
     import torch
     w = gemm_inputs.WORKLOADS[name]
     host_ops, dev_ops = _operands(w)
-    ref = _run(w, dev_ops)
+    ref = _run(w, dev_ops, config={"block_n": 256, "mode": 3})
     assert _plan(w, config={"block_n": 512})["mode"] == 6
     for s in (0, 2):
         assert torch.equal(_run(w, dev_ops, config={"block_n": 512, "mode": 6, "stages": s}), ref), f"stages={s}"

@@ -116,13 +116,19 @@ def test_stage_counts_bit_identical_bn192():
 def test_planner_tile_widths():
     """The planner's width choice counts whole waves of tiles: 2048^3 fills
     fewer SMs with 256-wide tiles than with 128-wide ones, but 128-wide tiles
-    stage twice the operand bytes per product, so 256 (paired) wins; a
-    1000^3 problem fits in one wave either way and keeps 128; a short K loop
-    keeps 128 for the epilogue's sake."""
+    stage twice the operand bytes per product, so 256 (paired) wins; 8192^3
+    with a long K loop takes the paired 256 x 512 tiles (mode 6), 4096^3 and
+    an fp32 output keep the 256-column pairs; a 1000^3 problem fits in one
+    wave either way and keeps 128; a short K loop keeps 128 for the
+    epilogue's sake."""
     p = _plan(2048, 2048, 2048, "f16", "f16")
     assert p["block_n"] == 256 and p["pair_mma"] == 1
     p = _plan(8192, 8192, 8192, "bf16", "bf16")
-    assert p["block_n"] == 256 and p["pair_mma"] == 1
+    assert p["block_n"] == 512 and p["mode"] == 6 and p["pair_mma"] == 1
+    p = _plan(4096, 4096, 4096, "f16", "f16")
+    assert p["block_n"] == 256 and p["mode"] == 3
+    p = _plan(8192, 8192, 8192, "bf16", "f32")
+    assert p["block_n"] == 256 and p["mode"] == 3
     assert _plan(1000, 1000, 1000, "f16", "f16")["block_n"] == 128
     assert _plan(8192, 8192, 256, "f16", "f16")["block_n"] == 128
 
@@ -213,7 +219,7 @@ def test_paired_slots_only_with_tma_operands():
     """Element-load staging (an A pitch that TMA cannot take) and the
     resident-B mode keep one barrier pair per slot."""
     import tensor_core_gemm_tma_gb300 as sg
-    assert _plan(8192, 8192, 8192, "bf16", "bf16")["ring_group"] == 2
+    assert _plan(4096, 4096, 4096, "bf16", "bf16")["ring_group"] == 2
     assert _plan(40000, 384, 96, "f16", "f16")["ring_group"] == 1      # mode 4
     lib = sg.load_library()
     M, N, K = 600, 500, 1000
