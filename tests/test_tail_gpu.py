@@ -103,11 +103,15 @@ def test_split_with_residual():
 
 
 def test_split_only_where_it_pays():
-    """No split for a last wave over half the clusters, for FP8 operands
-    (a half tile would not be whole 128-column boxes per CTA), for
-    128-column tiles, or for the resident-B mode."""
-    p = _plan(8192, 8192, 8192, "bf16", "bf16")            # 1024 tiles: 36 over 13 full waves of 76
-    assert p["block_n"] == 256 and p["tail_units"] == 72
+    """No split for a last wave over half the clusters, for FP8 operands in
+    256-column tiles (a half tile would not be whole 128-column boxes per
+    CTA), for 128-column tiles, or for the resident-B mode; 256 x 512 tiles
+    (mode 6) split into 256-column halves."""
+    p = _plan(8192, 8192, 8192, "bf16", "f32")             # 1024 tiles: 36 over 13 full waves of 76
+    assert p["block_n"] == 256 and p["mode"] == 3 and p["tail_units"] == 72
+    p = _plan(16384, 8192, 4096, "f16", "f16")              # 1024 wide tiles: 36 over 13 full waves
+    assert p["block_n"] == 512 and p["mode"] == 6 and p["tail_units"] == 72
+    assert _plan(8192, 8192, 8192, "bf16", "bf16")["tail_units"] == 0   # 512 wide tiles: 56 left
     assert _plan(4096, 4096, 4096, "f16", "f16")["tail_units"] == 56   # 256 tiles: 28 left
     assert _plan(8192, 8192, 8192, "e4m3", "bf16")["tail_units"] == 0
     assert _plan(40000, 384, 96, "f16", "f16")["tail_units"] == 0      # mode 4
@@ -116,13 +120,15 @@ def test_split_only_where_it_pays():
 
 
 def test_full_size_square8192_split_sampled():
-    """The bench's 8192^3 bf16 launch (split tail) on the last rows and
-    columns, where the half-width units land, against the oracle."""
+    """The 8192^3 bf16 product in paired 256 x 256 tiles (split tail) on the
+    last rows and columns, where the half-width units land, against the
+    oracle."""
     import gemm_inputs
     w = gemm_inputs.WORKLOADS["square8192_bf16"]
-    assert _plan(w.M, w.N, w.K, "bf16", "bf16")["tail_units"] > 0
     a, b = w.a_bits(), w.b_bits()
-    got = run_gpu(a, b, w.M, w.N, w.K, "bf16", "bf16")
+    with _Hooks(3, 1):
+        assert _plan(w.M, w.N, w.K, "bf16", "bf16")["tail_units"] > 0
+        got = run_gpu(a, b, w.M, w.N, w.K, "bf16", "bf16")
     rng = np.random.default_rng(11)
     rows = np.concatenate([rng.integers(w.M - 1024, w.M, 2000), rng.integers(0, w.M, 500)])
     cols = np.concatenate([rng.integers(w.N - 2048, w.N, 2000), rng.integers(0, w.N, 500)])
