@@ -245,16 +245,11 @@ typedef struct {
     int32_t ring_group;    /* ring slots filled and consumed together on one
                               pair of barriers (2 when both operands arrive by
                               TMA and the ring has 6 or 8 slots, else 1) */
-    int32_t tail_units;    /* units the last tiles of the raster were split
-                              into (0: none): when a last wave of 256-column
-                              tiles (16-bit operands, both by TMA) or of
-                              512-column tiles would fill at most half of the
-                              clusters, each of its tiles runs as two halves;
-                              when a last wave of 512-column tiles of 16-bit
-                              operands fills more than half but at most three
-                              quarters of them, half of the clusters' worth
-                              of its tiles run as halves and the rest as four
-                              128-column quarters each */
+    int32_t tail_units;    /* half-width units the last tiles of the raster
+                              were split into (0: none): when a last wave of
+                              256-column tiles (16-bit operands, both by TMA)
+                              would fill at most half of the clusters, each of
+                              its tiles runs as two 128-column units */
 } sg_plan_info;
 
 int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int epilogue, int stages,

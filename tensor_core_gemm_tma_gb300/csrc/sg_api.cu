@@ -249,7 +249,7 @@ struct Plan {
     int cm = 1;    // CTAs per cluster along M
     int stages = 0, max_stages = 0;
     int ring_group = 1;  // ring slots sharing one full and one empty barrier
-    int64_t units = 0, full_units = 0, half_units = 0;  // work units launched; whole tiles; halves (the rest: quarters)
+    int64_t units = 0, full_units = 0;  // work units launched; those of whole tiles (the rest: half tiles)
     int64_t m_blocks = 0, n_blocks = 0, tiles = 0, k_chunks = 0;
     int grid = 0;
     int smem = 0;
@@ -320,14 +320,10 @@ std::atomic<int> g_force_mode{[] {
 // Waves of `units` work units over `slots` clusters, the last wave counted
 // half when it would be split into half-width units (fills at most half of
 // the slots; see the tail split below).
-double wave_count(int64_t units, int64_t slots, bool splittable, bool quarters = false) {
+double wave_count(int64_t units, int64_t slots, bool splittable) {
     const int64_t full = units / slots, tail = units % slots;
     double w = static_cast<double>(full);
-    if (tail) {
-        if (splittable && full > 0 && 2 * tail <= slots) w += 0.5;
-        else if (quarters && full > 0 && 4 * tail <= 3 * slots) w += 0.75;
-        else w += 1.0;
-    }
+    if (tail) w += (splittable && full > 0 && 2 * tail <= slots) ? 0.5 : 1.0;
     return w;
 }
 
@@ -391,18 +387,22 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // instead of paired 256-column tiles when its waves cost less, counting
     // its per-SM throughput at full load as 1.08 of theirs (measured on
     // GB300: 8192^3 bf16 +7.9%, FP8 +3.9%, 16384 x 8192 x 4096 +3.3%,
-    // 6144 x 12288 x 4096 +1.4%, 8192^2 x 2048 +1.3%; 4096^3 -2% and 2048^3
-    // -29%, both rejected by the wave count).  Only with a long K loop (the
-    // tile boundary, where the second accumulator waits for the previous
-    // tile's epilogue to read it, then weighs little), a 16-bit output and no
-    // residual (there the epilogue hands the accumulator back before storing).
+    // 6144 x 12288 x 4096 +1.4%, 8192^2 x 2048 +1.3%; 4096^3 -2 to 0% and
+    // 2048^3 -29%, left out by requiring three full waves of wide tiles).
+    // Only with a long K loop (the tile boundary, where the second
+    // accumulator waits for the previous tile's epilogue to read it, then
+    // weighs little), a 16-bit output and no residual (there the epilogue
+    // hands the accumulator back before storing).
     bool auto_wide = false;
     if (mode == 3 && bn == 256 && !bn_forced && pl->k_chunks >= 32 && out_dtype != SG_F32 && !residual && a_tma &&
         b_tma && !decode) {
         const int64_t clusters = st.sm_count / 2, mc = cdiv(pl->m_blocks, 2);
+        const int64_t wide_tiles = mc * cdiv(N, 512);
         const double c3 = wave_count(mc * cdiv(N, 256), clusters, esz == 2) * 256.0;
-        const double c6 = wave_count(mc * cdiv(N, 512), clusters, true, esz == 2) * 512.0 / 1.08;
-        auto_wide = c6 < 0.98 * c3;
+        const double c6 = wave_count(wide_tiles, clusters, true) * 512.0 / 1.08;
+        // at least three full waves of wide tiles: with fewer (4096^3: 1.7)
+        // the estimate of the last wave was off by more than the margin
+        auto_wide = wide_tiles >= 3 * clusters && c6 < 0.98 * c3;
     }
     // Mode 4 (resident B) when B is small: at most 2 K chunks and 4 column
     // blocks of 128, so all of B fits next to a ring of at least 2 A tiles,
@@ -475,31 +475,14 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // over twice as many clusters and takes about half as long (the other
     // waves are unchanged).  Each output element is still computed by one
     // unit, summing the same products in the same K order: C keeps its bits.
-    //
-    // A 512-column tile of 16-bit operands (mode 6) can also be cut into four
-    // 128-column quarters: when the last wave fills more than half of the
-    // clusters but at most three quarters, half of the clusters' worth of
-    // its tiles run as halves (one wave of halves) and the rest as quarters
-    // (one wave of quarters), so that wave takes about three quarters of a
-    // tile's time instead of a whole one (8192^3: 56 tiles after 6 waves of
-    // 76 become 76 halves and 72 quarters).
     pl->units = pl->full_units = pl->tiles;
-    pl->half_units = 0;
     const int64_t tail = pl->tiles % clusters;
     const bool split_ok = g_tail_split.load() && !(choice && choice->tail_split < 0);
     const bool splittable = mode == 6 || (esz == 2 && bn == 256);  // halves of whole B boxes per CTA
-    const bool quarters = mode == 6 && esz == 2;                     // quarters of whole B boxes per CTA
-    if (split_ok && !panel && splittable && a_tma && b_tma && pl->k_chunks > 0 && pl->tiles > clusters && tail > 0) {
-        if (2 * tail <= clusters) {
-            pl->full_units = pl->tiles - tail;
-            pl->half_units = 2 * tail;
-            pl->units = pl->full_units + 2 * tail;
-        } else if (quarters && 4 * tail <= 3 * clusters) {
-            const int64_t halves = clusters / 2, quads = tail - halves;
-            pl->full_units = pl->tiles - tail;
-            pl->half_units = 2 * halves;
-            pl->units = pl->full_units + 2 * halves + 4 * quads;
-        }
+    if (split_ok && !panel && splittable && a_tma && b_tma && pl->k_chunks > 0 &&
+        pl->tiles > clusters && tail > 0 && 2 * tail <= clusters) {
+        pl->full_units = pl->tiles - tail;
+        pl->units = pl->full_units + 2 * tail;
     }
     pl->grid = static_cast<int>((pl->units < clusters ? pl->units : clusters) * cm);
     const int oes = elem_bytes(out_dtype);
@@ -666,7 +649,6 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.n_blocks = static_cast<int32_t>(pl.n_blocks);
     prm.num_tiles = static_cast<int32_t>(pl.units);
     prm.full_units = static_cast<int32_t>(pl.full_units);
-    prm.half_units = static_cast<int32_t>(pl.half_units);
     prm.k_chunks = static_cast<int32_t>(pl.k_chunks);
     prm.stages = pl.stages;
     prm.ring_group = pl.ring_group;

@@ -141,13 +141,11 @@ struct Params {
     int32_t M, N, K;
     int32_t m_blocks, n_blocks, num_tiles, k_chunks;  // num_tiles counts work units (below)
     // Work units: units below full_units are whole cluster tiles (CM row
-    // blocks by the tile width) in raster order; the next half_units units
-    // are the following tiles split into two halves each (left half first),
-    // and the units after those (mode 6 only) the last tiles split into four
-    // quarters each, so that a last wave spreads over more clusters.
-    // Without a split full_units == num_tiles.
+    // blocks by BN columns) in raster order; the tiles after them, the last
+    // ones of the raster, are each split into two units of BN / 2 columns
+    // (their left half first) so that a short last wave spreads over twice
+    // as many clusters.  Without a split full_units == num_tiles.
     int32_t full_units;
-    int32_t half_units;
     uint32_t idesc_half;   // tcgen05 instruction descriptor of a half-width unit
     int32_t stages;
     int32_t ring_group;    // ring slots filled and consumed together on one barrier pair (1 or 2)
@@ -271,13 +269,11 @@ __device__ __forceinline__ void tile_coords(int tile, const Params& p, uint32_t 
 
 // Row block and first column of work unit `u` (modes 1, 3, 6; TW is the
 // tile width); returns its width in columns.  Only 256-column tiles of
-// 16-bit operands and 512-column wide tiles are ever split into halves, and
-// only 512-column tiles of 16-bit operands into quarters: each piece is then
-// a whole number of 128-byte B boxes in every CTA.
+// 16-bit operands and 512-column wide tiles are ever split: each half is
+// then a whole number of 128-byte B boxes in every CTA.
 template <int CM, int TW, int ESZ>
 __device__ __forceinline__ int unit_coords(int u, const Params& p, uint32_t rank, int& mb, int& col0) {
     constexpr bool SPLITTABLE = (TW == 256 && ESZ == 2) || TW == 512;
-    constexpr bool QUARTERS = TW == 512 && ESZ == 2;
     int nb;
     if (!SPLITTABLE || u < p.full_units) {
         tile_coords<CM>(u, p, rank, mb, nb);
@@ -285,15 +281,9 @@ __device__ __forceinline__ int unit_coords(int u, const Params& p, uint32_t rank
         return TW;
     }
     const int v = u - p.full_units;
-    if (!QUARTERS || v < p.half_units) {
-        tile_coords<CM>(p.full_units + (v >> 1), p, rank, mb, nb);
-        col0 = nb * TW + (v & 1) * (TW / 2);
-        return TW / 2;
-    }
-    const int w = v - p.half_units;
-    tile_coords<CM>(p.full_units + (p.half_units >> 1) + (w >> 2), p, rank, mb, nb);
-    col0 = nb * TW + (w & 3) * (TW / 4);
-    return TW / 4;
+    tile_coords<CM>(p.full_units + (v >> 1), p, rank, mb, nb);
+    col0 = nb * TW + (v & 1) * (TW / 2);
+    return TW / 2;
 }
 
 // Wait for phase `parity` of `bar`, giving up after `limit` ns or when another
@@ -722,7 +712,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // paired: each accumulator's columns (sw of them) are split
                 // between the two CTAs, this CTA staging [rank * sw / 2, +sw / 2)
                 // of each in bps boxes
-                const int sw = (WIDE && width >= BN) ? BN : width;
+                const int sw = WIDE ? BN : width;
                 const int bps = (sw / 2) / G::BOXC;
                 for (int kc = 0; kc < fills; kc += grp, it += grp) {
                     if (!wait_bounded(empty_bar(slot), phase ^ 1u, abort_flag, p.status, p.wait_limit_ns,
@@ -846,9 +836,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 int umb, ucol;
                 const int uw = unit_coords<CM, TW, ESZ>(tile, p, rank, umb, ucol);
-                // accumulators this unit fills (a quarter of a wide tile: one, 128 columns of it)
-                const int nsub = (WIDE && uw > BN) ? uw / BN : 1;
-                const uint32_t idesc = uw >= BN ? p.idesc : p.idesc_half;
+                const int nsub = WIDE ? uw / BN : 1;  // accumulators this unit fills
+                const uint32_t idesc = (WIDE || uw == BN) ? p.idesc : p.idesc_half;
                 // the unit's accumulators in rotation order; the first is claimed
                 // now, the others just before their first MMA
                 uint32_t sab[NSUB] = {}, saph[NSUB] = {};
@@ -1009,9 +998,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int mb = tile, ucol = sub * BN, width = BN;
             if constexpr (WIDE) {
                 int u0;
-                const int uw = unit_coords<CM, TW, ESZ>(tile, p, rank, mb, u0);
-                subs = uw > BN ? uw / BN : 1;
-                width = uw < BN ? uw : BN;
+                subs = unit_coords<CM, TW, ESZ>(tile, p, rank, mb, u0) / BN;
                 ucol = u0 + sub * BN;
             } else if constexpr (!PANEL) {
                 width = unit_coords<CM, TW, ESZ>(tile, p, rank, mb, ucol);
@@ -1040,7 +1027,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < NCH; ++i) {
                     const int c = part * COLS + i * SPLIT * COLS;
-                    if (c >= width) break;  // a quarter unit: only its 128 columns hold its products
                     uint32_t r[32], r2[32];
                     tmem_ld_32x32b_x32(t_row + c, r);
                     tmem_ld_32x32b_x32(t_row + c + 32, r2);
@@ -1069,9 +1055,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < NCH; ++i) {
-                    const int c = part * COLS + i * SPLIT * COLS;
-                    const int col0 = ucol + c;
-                    if (c < width && row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
+                    const int col0 = ucol + part * COLS + i * SPLIT * COLS;
+                    if (row0 < p.M && col0 < p.N) {  // warp-uniform: the box holds in-range elements
                         if (leader) bulk_wait_group_read<0>();  // the previous store has read the buffer
                         __syncwarp();
                         const uint32_t rowaddr = buf + lane * 128;

