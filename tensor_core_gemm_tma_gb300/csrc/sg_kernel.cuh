@@ -27,20 +27,6 @@
 //
 // Five modes (MODE; the numbers are those of sg_plan_info.mode):
 //   1  one CTA per 128 x BN tile.
-//   4  resident B ("decoded panels", Tolk.Stage): for a small K x N, each
-//      CTA stages all of B once (every K chunk of every 128-column block)
-//      and streams only A, one 128-row tile per ring slot; the MMAs of
-//      every column block of that row tile read the one A slot, each into
-//      its own rotating accumulator.  Tile units are (row tile, column
-//      block) in that order; the epilogue is the same as mode 1's.
-//   6  wide paired tiles: mode 3 with a 256 x 2BN tile (BN = 256) held as
-//      two BN-wide accumulators.  Each CTA stages its 128 rows of A once per
-//      K chunk for both accumulators and its half of each accumulator's B
-//      columns, so a K chunk moves 48 KiB per CTA for 128 x 512 x 64
-//      products instead of 32 KiB for 128 x 256 x 64 (a quarter fewer
-//      operand bytes per product).  The tile's second accumulator is claimed
-//      only after the first one's first MMAs are issued, so the epilogue of
-//      the previous tile drains it meanwhile.
 //   3  paired MMA (tcgen05 cta_group::2): the two CTAs of a cluster compute
 //      one 256 x BN tile.  Each CTA stages its own 128 rows of A and its own
 //      BN/2 columns of B (so a stage is 32 KiB instead of 48 KiB for
@@ -50,6 +36,12 @@
 //      its commits free the ring slots and hand accumulators to the
 //      epilogues of both CTAs; both epilogues release accumulators on the
 //      even CTA's barrier.
+//   4  resident B ("decoded panels", Tolk.Stage): for a small K x N, each
+//      CTA stages all of B once (every K chunk of every 128-column block)
+//      and streams only A, one 128-row tile per ring slot; the MMAs of
+//      every column block of that row tile read the one A slot, each into
+//      its own rotating accumulator.  Tile units are (row tile, column
+//      block) in that order; the epilogue is the same as mode 1's.
 //   5  decoded panel: mode 4 with B given as int8 codes and one fp32 scale
 //      per column.  At CTA start the eight epilogue warps decode all of B
 //      into the resident panel, each code to the 16-bit value equal to it,
@@ -57,6 +49,16 @@
 //      host": the panel is decoded once and read back by every trip of the
 //      other output loop); the epilogue multiplies by the column's scale,
 //      fused with the bias.
+//   6  wide paired tiles: mode 3 with a 256 x 2BN tile (BN = 256) held as
+//      two BN-wide accumulators.  Each CTA stages its 128 rows of A once per
+//      K chunk for both accumulators and its half of each accumulator's B
+//      columns, so a K chunk moves 48 KiB per CTA for 128 x 512 x 64
+//      products instead of 32 KiB for 128 x 256 x 64 (a quarter fewer
+//      operand bytes per product).  The tile's second accumulator is claimed
+//      only after the first one's first MMAs are issued, and the epilogue
+//      (16-bit output, no residual) hands each accumulator back as soon as
+//      its values are in registers, before storing them: the tile boundary
+//      waits only for those reads.
 //
 // The ring generalises the two-slot pipeline of Tolk.Stage (copy chunk k+1
 // into slot (k+1) mod 2 while computing on slot k mod 2) and the `stages`
