@@ -77,6 +77,7 @@ def parse():
                          "or the write alone (its dirty lines are written back during the timed launch)")
     ap.add_argument("--block-n", type=int, default=0, help="sg_config.block_n (0: the planner's)")
     ap.add_argument("--mode", type=int, default=0, help="sg_config.mode (0: the planner's)")
+    ap.add_argument("--group-m", type=int, default=0, help="sg_config.group_m, the raster group (0: the planner's)")
     return ap.parse_args()
 
 
@@ -605,8 +606,8 @@ def main():
     clocks = ClockSampler(cvd.split(",")[local] if cvd else local)
     host_inputs = device_inputs(w, device)
     cfg = None
-    if args.block_n or args.mode:
-        cfg = {"block_n": args.block_n, "mode": args.mode}
+    if args.block_n or args.mode or args.group_m:
+        cfg = {"block_n": args.block_n, "mode": args.mode, "group_m": args.group_m}
     # warm-up + timed steps (the clock sampler runs over the timed region)
     with clocks:
         barrier()
