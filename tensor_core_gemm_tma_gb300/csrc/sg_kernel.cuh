@@ -256,7 +256,9 @@ __device__ __forceinline__ void copy_b_elements(uint32_t dst, const Params& p, i
 
 // Linear cluster-tile index -> (row block of this CTA, column block), with a
 // grouped raster over cluster row blocks (CM row blocks each): group_m of
-// them are swept together for L2 reuse.
+// them are swept together for L2 reuse.  Odd groups sweep the column blocks
+// backwards, so a group starts on the B columns the previous one ended on,
+// which are still in L2.
 template <int CM>
 __device__ __forceinline__ void tile_coords(int tile, const Params& p, uint32_t rank, int& mb, int& nb) {
     const int mc_blocks = (p.m_blocks + CM - 1) / CM;
@@ -267,6 +269,7 @@ __device__ __forceinline__ void tile_coords(int tile, const Params& p, uint32_t 
     const int r = tile - g * per_group;
     mb = (first_m + r % gsize) * CM + static_cast<int>(rank);
     nb = r / gsize;
+    if (g & 1) nb = p.n_blocks - 1 - nb;
 }
 
 // Row block and first column of work unit `u` (modes 1, 3, 6; TW is the
