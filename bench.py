@@ -691,7 +691,7 @@ def secondaries(sg, device, stream, peaks, args):
         lr = None if args.no_library_reference or config is not None else \
             library_reference(ws, dt, stream, flush_mode=args.flush)
         del dt
-        p = sg.plan(ws.M, ws.N, ws.K, out_dt_in(ws), out_torch_dtype(ws), ws.epilogue, config=config) \
+        p = sg.plan(ws.M, ws.N, ws.K, in_torch_dtype(ws), out_torch_dtype(ws), ws.epilogue, config=config) \
             if not ws.b_coded else None
         e = {"workload": ws.name, "ms_per_step": m, "TFLOP/s": ws.flops / (m * 1e-3) / 1e12,
              "roofline": roofline_of(ws, m, peaks, recorded_traffic(ws.name) if config is None else None, lr)}
@@ -721,7 +721,7 @@ def secondaries(sg, device, stream, peaks, args):
     return out
 
 
-def out_dt_in(w):
+def in_torch_dtype(w):
     import torch
     return {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}[w.in_dtype]
 

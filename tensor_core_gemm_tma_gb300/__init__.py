@@ -52,9 +52,11 @@ class PlanInfo(ctypes.Structure):
 
 class Config(ctypes.Structure):
     """sg_config: an explicit launch configuration (0 = the planner's choice
-    for that field).  block_n 128/192/256; mode 1 (one CTA per tile), 3 (CTA
-    pairs with the paired MMA, each CTA owning 128 x block_n) or 4 (resident
-    B); stages 1..8; group_m 1..64; tail_split -1 (never) or 0/1 (default)."""
+    for that field).  block_n 128/192/256/512; mode 1 (one CTA per tile), 3
+    (CTA pairs with the paired MMA, each CTA owning 128 x block_n), 4
+    (resident B) or 6 (CTA pairs over 256 x 512 tiles held as two 256-column
+    accumulators; block_n 512); stages 1..8; group_m 1..64; tail_split -1
+    (never) or 0/1 (default)."""
     _fields_ = [(n, ctypes.c_int32) for n in ("block_n", "mode", "stages", "group_m", "tail_split")]
 
 
