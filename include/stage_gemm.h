@@ -263,8 +263,8 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
  * same bits whatever the configuration (gizml:tile, "tune": every
  * configuration computes the same result; Tolk.Stage: staging never rounds).
  *
- *   block_n     output tile columns: 128, 192 or 256 (FP8 operands: 128 or
- *               256, whole 128-byte B boxes).
+ *   block_n     output tile columns: 128, 192, 256 or 512 (FP8 operands:
+ *               128, 256 or 512, whole 128-byte B boxes); 512 is mode 6.
  *   mode        1: one CTA per 128 x block_n output tile.
  *               3: the two CTAs of a cluster compute one 256 x block_n tile
  *                  with the paired MMA (tcgen05 cta_group::2); each CTA owns
@@ -274,11 +274,17 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
  *                  and B must be TMA-legal.
  *               4: B resident in shared memory (block_n 128; K at most two
  *                  128-byte stages of K, N at most 512; A and B TMA-legal).
+ *               6: as 3 over 256 x 512 tiles held as two 256-column
+ *                  accumulators (block_n 512): each CTA stages its A rows
+ *                  once for both, a quarter fewer operand bytes per product
+ *                  than 256-column pairs; A and B must be TMA-legal.
  *   stages      operand ring depth, 1..SG_MAX_STAGES (0: the deepest that
  *               fits); a depth that does not fit is SG_ERR_STAGES.
- *   group_m     tile raster: cluster row blocks swept together, 1..64.
- *   tail_split  1 or 0: split a short last wave of 256-column tiles into
- *               128-column units where it pays (the default); -1: never.
+ *   group_m     tile raster: cluster row blocks swept together, 1..64 (odd
+ *               groups sweep the column blocks backwards).
+ *   tail_split  1 or 0: split a short last wave of 256- or 512-column tiles
+ *               into half-width units where it pays (the default); -1:
+ *               never.
  *
  * The gizml:tile program's workgroup per 128 x 128 output tile is
  * {block_n = 128, mode = 1} (one CTA per tile) or {block_n = 128, mode = 3}
