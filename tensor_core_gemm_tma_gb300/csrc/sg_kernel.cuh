@@ -915,6 +915,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     }
                                 }
                             }
+                            // A wide tile's earlier accumulators are complete once their
+                            // last MMAs are: hand each to the epilogue before the next
+                            // accumulator's last MMAs, so its reads overlap them and the
+                            // next tile's first MMAs find it free.
+                            if (WIDE && h + 1 < nsub && kc + ring_group >= p.k_chunks) {
+                                umma_commit_pair_multicast(tfull_bar(sab[h]), CLUSTER_MASK);
+                            }
                         }
                     }
                     if (!ok) break;
@@ -933,15 +940,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 if (issuer) {
-#pragma unroll
-                    for (int h = 0; h < NSUB; ++h) {
-                        if (h < nsub) {
-                            if constexpr (PAIR) {
-                                umma_commit_pair_multicast(tfull_bar(sab[h]), CLUSTER_MASK);  // both CTAs' epilogues
-                            } else {
-                                umma_commit(tfull_bar(sab[h]));
-                            }
-                        }
+                    // the unit's last accumulator (a wide tile's earlier one was handed over above)
+                    const uint32_t last = nsub > 1 ? sab[NSUB - 1] : sab[0];
+                    if constexpr (PAIR) {
+                        umma_commit_pair_multicast(tfull_bar(last), CLUSTER_MASK);  // both CTAs' epilogues
+                    } else {
+                        umma_commit(tfull_bar(last));
                     }
                 }
             }
