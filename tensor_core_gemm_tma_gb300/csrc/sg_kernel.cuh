@@ -54,11 +54,12 @@
 //      K chunk for both accumulators and its half of each accumulator's B
 //      columns, so a K chunk moves 48 KiB per CTA for 128 x 512 x 64
 //      products instead of 32 KiB for 128 x 256 x 64 (a quarter fewer
-//      operand bytes per product).  The tile's second accumulator is claimed
-//      only after the first one's first MMAs are issued, and the epilogue
-//      (16-bit output, no residual) hands each accumulator back as soon as
-//      its values are in registers, before storing them: the tile boundary
-//      waits only for those reads.
+//      operand bytes per product).  The first accumulator goes to the
+//      epilogue before the second one's last MMAs, the next tile claims its
+//      second accumulator only after its first one's first MMAs are issued,
+//      and the epilogue (16-bit output, no residual) hands each accumulator
+//      back as soon as its values are in registers, before storing them:
+//      the tile boundary waits only for those reads, which overlap MMAs.
 //
 // The ring generalises the two-slot pipeline of Tolk.Stage (copy chunk k+1
 // into slot (k+1) mod 2 while computing on slot k mod 2) and the `stages`
