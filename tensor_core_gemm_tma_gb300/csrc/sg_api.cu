@@ -261,10 +261,11 @@ struct Plan {
 // Modes 4 and 5's shared memory: the resident B (k_chunks x n_blocks blocks
 // of bn columns by 128 bytes of K), a ring of A tiles (k_chunks chunks
 // each), the staging buffers, mode 5's per-column scales and biases (fp32,
-// n_blocks * bn of each) and the barriers.
-int64_t smem_panel(int bn, int stages, int64_t k_chunks, int64_t n_blocks, bool decode = false) {
+// n_blocks * bn of each) or mode 4's biases (with a bias), and the barriers.
+int64_t smem_panel(int bn, int stages, int64_t k_chunks, int64_t n_blocks, bool decode = false, bool bias = false) {
     return k_chunks * n_blocks * bn * sg::BK_BYTES + stages * k_chunks * sg::A_STAGE_BYTES +
-           sg::EPI_WARPS * sg::EPI_BUF_BYTES + (decode ? n_blocks * bn * 8 : 0) + sg::BAR_AREA + sg::SMEM_ALIGN;
+           sg::EPI_WARPS * sg::EPI_BUF_BYTES + (decode ? n_blocks * bn * 8 : bias ? n_blocks * bn * 4 : 0) +
+           sg::BAR_AREA + sg::SMEM_ALIGN;
 }
 
 int smem_for(int bn, int stages, int mode) {
@@ -329,7 +330,7 @@ double wave_count(int64_t units, int64_t slots, bool splittable) {
 
 int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, const void* C,
               int64_t ldc, int stages, bool a_tma, bool b_tma, Plan* pl, const Choice* choice = nullptr,
-              bool decode = false, bool residual = false) {
+              bool decode = false, bool residual = false, bool bias = false) {
     const int esz = elem_bytes(in_dtype);
     const int boxc = 128 / esz;  // B columns per 128-byte box: tile widths and CTA shares are multiples
     pl->a_tma = a_tma ? 1 : 0;
@@ -409,7 +410,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // and there are enough row tiles to keep every SM busy.
     const int64_t nb128 = cdiv(N, 128);
     const bool panel_ok = a_tma && b_tma && pl->k_chunks <= 2 && nb128 <= 4 &&
-                          smem_panel(128, 2, pl->k_chunks, nb128) <= st.smem_optin;
+                          smem_panel(128, 2, pl->k_chunks, nb128, false, bias) <= st.smem_optin;
     if (panel_ok && pl->m_blocks >= st.sm_count && !bn_forced) mode = 4;
     auto legal = [&](int m) {
         return m == 1 || (m == 3 && pairable) || (m == 4 && panel_ok) || (m == 6 && bn == 256 && a_tma && b_tma);
@@ -443,7 +444,8 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     pl->tiles = panel ? pl->m_blocks : cdiv(pl->m_blocks, cm) * pl->n_blocks;
     int maxs = 0;
     for (int s = 1; s <= SG_MAX_STAGES; ++s) {
-        const int64_t need = panel ? smem_panel(bn, s, pl->k_chunks, pl->n_blocks, mode == 5) : smem_for(bn, s, mode);
+        const int64_t need =
+            panel ? smem_panel(bn, s, pl->k_chunks, pl->n_blocks, mode == 5, bias) : smem_for(bn, s, mode);
         if (need <= st.smem_optin) maxs = s;
     }
     pl->max_stages = maxs;
@@ -461,7 +463,7 @@ int make_plan(const DevState& st, int64_t M, int64_t N, int64_t K, int in_dtype,
     // barrier counts; the grouping never changes which MMAs run or their
     // order, so C keeps its bits.
     pl->ring_group = (!panel && a_tma && b_tma && stages >= 6 && stages % 2 == 0) ? 2 : 1;
-    pl->smem = panel ? static_cast<int>(smem_panel(bn, stages, pl->k_chunks, pl->n_blocks, mode == 5))
+    pl->smem = panel ? static_cast<int>(smem_panel(bn, stages, pl->k_chunks, pl->n_blocks, mode == 5, bias))
                      : smem_for(bn, stages, mode);
     pl->tmem_cols = sg::TMEM_COLS;
     // Two CTAs on one SM would each hold half the tensor memory or wait for
@@ -617,7 +619,8 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
         lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, a_tma, b_tma, c_tma_legal(C, M, ldc, out_dtype), &tuned))
         choice = &tuned;
     Plan pl;
-    int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice, decode, R != nullptr);
+    int rc = make_plan(st, M, N, K, in_dtype, out_dtype, C, ldc, stages, a_tma, b_tma, &pl, choice, decode, R != nullptr,
+                       epilogue == SG_EPI_BIAS_RELU);
     if (rc != SG_OK) return rc;
     if (choice && choice->strict && !honours(pl, *choice)) return SG_ERR_CONFIG;
     if (used) *used = pl;
@@ -851,8 +854,8 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
     Choice tuned;
     const bool have = lookup_tuned(M, N, K, in_dtype, out_dtype, epilogue, true, true,
                                    c_tma_legal(C, M, ldc, out_dtype), &tuned);
-    if ((rc = make_plan(*st, M, N, K, in_dtype, out_dtype, C, ldc, stages, true, true, &pl, have ? &tuned : nullptr)) !=
-        SG_OK)
+    if ((rc = make_plan(*st, M, N, K, in_dtype, out_dtype, C, ldc, stages, true, true, &pl, have ? &tuned : nullptr,
+                        false, false, epilogue == SG_EPI_BIAS_RELU)) != SG_OK)
         return rc;
     fill_info(pl, info);
     return SG_OK;
@@ -913,7 +916,8 @@ int sg_plan_ex(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int
                                 &tuned))
         choice = &tuned;
     Plan pl;
-    if ((rc = make_plan(*st, M, N, K, in_dtype, out_dtype, C, ldc, stages, true, true, &pl, choice)) != SG_OK)
+    if ((rc = make_plan(*st, M, N, K, in_dtype, out_dtype, C, ldc, stages, true, true, &pl, choice, false, false,
+                        epilogue == SG_EPI_BIAS_RELU)) != SG_OK)
         return rc;
     if (given && !honours(pl, c)) return SG_ERR_CONFIG;
     fill_info(pl, info);

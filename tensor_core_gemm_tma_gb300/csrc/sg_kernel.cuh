@@ -509,6 +509,24 @@ __device__ __forceinline__ void scale_bias_smem(float (&v)[COLS], uint32_t par, 
     }
 }
 
+// + bias[col] for the COLS columns starting at col0, from the copy of the
+// biases staged in shared memory at `par` (zero past N; col0 + COLS lies
+// within the staged columns).
+template <int COLS>
+__device__ __forceinline__ void add_bias_smem(float (&v)[COLS], uint32_t par, int col0) {
+#pragma unroll
+    for (int i = 0; i < COLS / 4; ++i) {
+        float b0, b1, b2, b3;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b0), "=f"(b1), "=f"(b2), "=f"(b3)
+                     : "r"(par + static_cast<uint32_t>(col0 + 4 * i) * 4u));
+        v[4 * i + 0] += b0;
+        v[4 * i + 1] += b1;
+        v[4 * i + 2] += b2;
+        v[4 * i + 3] += b3;
+    }
+}
+
 // + bias[col] for the COLS columns starting at col0 (zero past N).
 template <int COLS>
 __device__ __forceinline__ void add_bias(float (&v)[COLS], const float* __restrict__ bias, int col0, int N) {
@@ -572,7 +590,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ring_group = (p.ring_group == 2 && stages % 2 == 0 && p.a_tma && p.b_tma) ? 2 : 1;
     // Shared-memory map.  Modes 1-3: [ring][staging][barriers].  Modes 4
     // and 5: [resident B: k_chunks x n_blocks blocks of BN columns][ring of A
-    // tiles, each k_chunks A chunks][staging][mode 5: scales, biases][barriers].
+    // tiles, each k_chunks A chunks][staging][mode 5: scales, biases; mode 4
+    // with a bias: biases][barriers].
     constexpr int B_BLOCK_BYTES = (BN / G::BOXC) * G::B_BOX_BYTES;  // one K chunk of one column block
     const uint32_t res_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks * p.n_blocks) * B_BLOCK_BYTES : 0u;
     const uint32_t stage_bytes = PANEL ? static_cast<uint32_t>(p.k_chunks) * A_STAGE_BYTES : L::STAGE_BYTES;
@@ -580,8 +599,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t epi_off = res_bytes + static_cast<uint32_t>(stages) * stage_bytes;
     // mode 5: per-column scales then biases, fp32, n_blocks * BN of each
     const uint32_t par_nbias = DECODE ? static_cast<uint32_t>(p.n_blocks) * BN * 4u : 0u;
+    // mode 4 with a bias: the biases alone, read from shared memory by every
+    // tile (a bias read from global memory per chunk cost its whole latency)
+    const bool bias_smem = PANEL && !DECODE && p.epi == SG_EPI_BIAS_RELU;
+    const uint32_t par_bias = bias_smem ? static_cast<uint32_t>(p.n_blocks) * BN * 4u : 0u;
     const uint32_t par_off = epi_off + EPI_WARPS * EPI_BUF_BYTES;
-    const uint32_t bar_off = par_off + 2u * par_nbias;
+    const uint32_t bar_off = par_off + 2u * par_nbias + par_bias;
 
     const uint32_t bar0 = base + bar_off;
     // barrier slots: full[0..7], empty[8..15], tmem_full[16..19], tmem_empty[20..23], drain[24],
@@ -1000,6 +1023,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // all eight epilogue warps have written their share before any reads it
             asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32) : "memory");
         }
+        if (bias_smem) {
+            // mode 4's biases (zero past N), read by every chunk of every tile
+            for (int i = e * 32 + lane; i < p.n_blocks * BN; i += EPI_WARPS * 32) {
+                const float bi = i < p.N ? __ldg(p.bias + i) : 0.0f;
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + par_off + 4u * i), "f"(bi) : "memory");
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(EPI_WARPS * 32) : "memory");
+        }
         uint32_t ab = 0, aph = 0;
         // accumulators: one per unit (modes 1, 3), one per column block of a row
         // tile (modes 4, 5), one per BN columns of a unit (mode 6)
@@ -1136,6 +1167,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if constexpr (DECODE) {
                     scale_bias_smem<COLS>(v, base + par_off, par_nbias, col0);
+                } else if (bias_smem) {
+                    add_bias_smem<COLS>(v, base + par_off, col0);
                 } else if (p.epi == SG_EPI_BIAS_RELU) {
                     add_bias<COLS>(v, p.bias, col0, p.N);
                 }

@@ -84,3 +84,31 @@ def test_panel_fp8():
 def test_panel_is_the_default_for_the_skinny_projection():
     p = _plan(518400, 384, 96, "f16", "f16")
     assert p["tiles"] == 4050 and p["block_n"] == 128 and p["mode"] == 4
+
+
+@pytest.mark.parametrize("in_dt,out_dt,M,N,K", [("e4m3", "bf16", 2500, 384, 200), ("f16", "f32", 1500, 300, 96),
+                                                ("bf16", "bf16", 700, 130, 64)])
+def test_panel_bias_from_shared_memory(in_dt, out_dt, M, N, K):
+    """Mode 4 stages the biases in shared memory once per CTA (zero past N)
+    and adds them per chunk from there: the same fp32 additions as the
+    single-CTA mode's reads from global memory, so the same bits."""
+    dist = ("normal", 0.0, 2.0) if in_dt == "e4m3" else ("normal", 0.0, 1.0)
+    a, b = seeded_case(M, N, K, in_dt, seed=114 + N, dist=dist)
+    bias = np.linspace(-2, 2, N).astype(np.float32)
+    assert _forced(4, lambda: _plan(M, N, K, in_dt, out_dt))["mode"] == 4
+    got4 = _forced(4, lambda: run_gpu(a, b, M, N, K, in_dt, out_dt, "bias_relu", bias))
+    got1 = _forced(1, lambda: run_gpu(a, b, M, N, K, in_dt, out_dt, "bias_relu", bias))
+    assert np.array_equal(got4, got1)
+    ref, _, S = oracle.gemm(a, b, in_dt, out_dt, "bias_relu", bias, K=K, N=N)
+    compare(got4, ref, S, out_dt, f"panel bias {in_dt} {M}x{N}x{K}")
+
+
+def test_panel_residual_with_bias():
+    M, N, K = 2000, 200, 96
+    a, b = seeded_case(M, N, K, "f16", seed=115)
+    r = _rbits(M, N, "f16", 115)
+    bias = np.linspace(-1, 1, N).astype(np.float32)
+    got4 = _forced(4, lambda: run_residual(a, b, r, M, N, K, "f16", "f16", "bias_relu", bias))
+    got1 = _forced(1, lambda: run_residual(a, b, r, M, N, K, "f16", "f16", "bias_relu", bias))
+    assert np.array_equal(got4, got1)
+    check(got4, a, b, r, "f16", "f16", "bias_relu", bias, what="panel residual + bias")
