@@ -112,3 +112,16 @@ def test_panel_residual_with_bias():
     got1 = _forced(1, lambda: run_residual(a, b, r, M, N, K, "f16", "f16", "bias_relu", bias))
     assert np.array_equal(got4, got1)
     check(got4, a, b, r, "f16", "f16", "bias_relu", bias, what="panel residual + bias")
+
+
+def test_panel_plan_counts_the_staged_biases():
+    """With a bias, mode 4's shared memory also holds the N biases (fp32,
+    whole 128-column blocks): the projection's plan grows by 3 x 128 x 4
+    bytes and keeps its 3 ring slots."""
+    import torch
+    import tensor_core_gemm_tma_gb300 as sg
+    plain = sg.plan(518400, 384, 96, torch.float16, torch.float16, "relu")
+    biased = sg.plan(518400, 384, 96, torch.float16, torch.float16, "bias_relu")
+    assert plain["mode"] == biased["mode"] == 4
+    assert biased["smem_bytes"] == plain["smem_bytes"] + 3 * 128 * 4
+    assert biased["stages"] == plain["stages"] == 3
