@@ -125,3 +125,17 @@ def test_panel_plan_counts_the_staged_biases():
     assert plain["mode"] == biased["mode"] == 4
     assert biased["smem_bytes"] == plain["smem_bytes"] + 3 * 128 * 4
     assert biased["stages"] == plain["stages"] == 3
+
+
+def test_panel_k_zero_gives_relu_bias():
+    """Program.fold: with K = 0 no MMA runs and every element is the
+    epilogue of zero: relu(bias[col]), read from the biases mode 4 staged in
+    shared memory (N = 296: the last 128-column block is ragged)."""
+    M, N = 1000, 296
+    bias = np.linspace(-3, 3, N).astype(np.float32)
+    a = np.zeros((M, 8), np.uint16)
+    b = np.zeros((8, N), np.uint16)
+    assert _forced(4, lambda: _plan(M, N, 0, "f16", "f16"))["mode"] == 4
+    got = _forced(4, lambda: run_gpu(a, b, M, N, 0, "f16", "f16", "bias_relu", bias))
+    want = np.tile(np.maximum(bias.astype(np.float64), 0), (M, 1))
+    assert np.array_equal(got, want.astype(np.float16).view(np.uint16))
