@@ -231,7 +231,8 @@ typedef struct {
     int32_t tiles;         /* output tiles */
     int32_t grid;          /* persistent CTAs launched */
     int32_t threads;       /* threads per CTA */
-    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t smem_bytes;    /* dynamic shared memory per CTA (modes 4 and 5:
+                              with a bias, the biases too) */
     int32_t tmem_columns;  /* tensor-memory columns allocated per CTA */
     int32_t tma_store;     /* 1: C written by TMA stores, 0: masked stores */
     int32_t cluster_m;     /* CTAs per cluster (1 or 2) */
@@ -241,7 +242,8 @@ typedef struct {
     int32_t group_m;       /* cluster row blocks swept together by the tile raster */
     int32_t mode;          /* 1 single CTA, 3 paired MMA, 4 B resident in
                               shared memory, 5 integer-coded B decoded into
-                              shared memory (2 is not used) */
+                              shared memory, 6 paired 256 x 512 tiles held as
+                              two 256-column accumulators (2 is not used) */
     int32_t ring_group;    /* ring slots filled and consumed together on one
                               pair of barriers (2 when both operands arrive by
                               TMA and the ring has 6 or 8 slots, else 1) */
@@ -273,7 +275,8 @@ int sg_plan(int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int ep
  *                  CTA (128 or 256 for 16-bit operands, 256 for FP8), and A
  *                  and B must be TMA-legal.
  *               4: B resident in shared memory (block_n 128; K at most two
- *                  128-byte stages of K, N at most 512; A and B TMA-legal).
+ *                  128-byte stages of K, N at most 512; A and B TMA-legal);
+ *                  with a bias, the biases are staged there too.
  *               6: as 3 over 256 x 512 tiles held as two 256-column
  *                  accumulators (block_n 512): each CTA stages its A rows
  *                  once for both, a quarter fewer operand bytes per product
