@@ -359,6 +359,42 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// C without a TMA-legal layout: the warp's 32 x COLS block, already in its
+// staging buffer in the TMA store's layout (row r at r * 128 bytes, 16-byte
+// chunk j at chunk j ^ (r mod 8)), is written one row at a time, lane l
+// taking columns l, l + 32, ...: each store instruction writes consecutive
+// elements of one row.  Elements past M or N are not written.  Not inlined:
+// the kernel's other paths keep the registers this fallback would take.
+template <int OUT, int COLS>
+static __device__ __noinline__ void store_rows(const Params& p, uint32_t buf, int row0, int col0, int lane) {
+    constexpr int EB = (OUT == SG_F32) ? 4 : 2;  // output bytes per element
+#pragma unroll 4
+    for (int r = 0; r < 32; ++r) {
+        const int row = row0 + r;
+        if (row >= p.M) break;  // warp-uniform; the rows after it are past M too
+#pragma unroll
+        for (int h = 0; h < COLS / 32; ++h) {
+            const int e = h * 32 + lane;
+            const int col = col0 + e;
+            if (col < p.N) {
+                const uint32_t byte = static_cast<uint32_t>(e * EB);
+                const uint32_t addr = buf + static_cast<uint32_t>(r) * 128u +
+                                      (((byte >> 4) ^ static_cast<uint32_t>(r & 7)) << 4) + (byte & 15u);
+                const int64_t idx = static_cast<int64_t>(row) * p.ldc + col;
+                if constexpr (OUT == SG_F32) {
+                    float x;
+                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x) : "r"(addr));
+                    static_cast<float*>(p.C)[idx] = x;
+                } else {
+                    unsigned short x;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(x) : "r"(addr));
+                    static_cast<unsigned short*>(p.C)[idx] = x;
+                }
+            }
+        }
+    }
+}
+
 template <int OUT>
 __device__ __forceinline__ float load_one(const void* X, int64_t idx) {
     if constexpr (OUT == SG_F32) {
@@ -402,17 +438,6 @@ __device__ __forceinline__ void add_staged_residual(float (&v)[COLS], uint32_t r
                 v[8 * j + 2 * t + 1] += hi;
             }
         }
-    }
-}
-
-template <int OUT>
-__device__ __forceinline__ void store_one(void* C, int64_t idx, float v) {
-    if constexpr (OUT == SG_F32) {
-        static_cast<float*>(C)[idx] = v;
-    } else if constexpr (OUT == SG_F16) {
-        static_cast<__half*>(C)[idx] = __float2half_rn(v);
-    } else {
-        static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
     }
 }
 
@@ -1214,14 +1239,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             bulk_commit_group();
                         }
                     }
-                } else if (row < p.M) {
+                } else if (row0 < p.M && col0 < p.N) {  // warp-uniform
+                    // C without a TMA-legal layout: the block goes through the
+                    // staging buffer in the same layout (the ReLU is already
+                    // applied), then out row by row
+                    const uint32_t rowaddr = buf + lane * 128;
 #pragma unroll
-                    for (int i = 0; i < COLS; ++i) {
-                        const int col = col0 + i;
-                        if (col < p.N) store_one<OUT>(p.C, static_cast<int64_t>(row) * p.ldc + col, v[i]);
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            if constexpr (OUT == SG_F32) {
+                                w[t] = __float_as_uint(v[4 * j + t]);
+                            } else {
+                                w[t] = pack2<OUT>(v[8 * j + 2 * t], v[8 * j + 2 * t + 1]);
+                            }
+                        }
+                        st_shared_v4(rowaddr + ((j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
                     }
+                    __syncwarp();
+                    store_rows<OUT, COLS>(p, buf, row0, col0, lane);
                 }
-                __syncwarp();  // the next tcgen05.ld is warp-collective
+                __syncwarp();  // the next tcgen05.ld is warp-collective; the buffer has been read
                 // the next chunk's residual (the store just issued must read the buffer first)
                 const int cn = c + SPLIT * COLS;
                 if (r_staged && cn < width && row0 < p.M && ucol + cn < p.N) load_residual(row0, ucol + cn);
