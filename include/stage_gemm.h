@@ -125,8 +125,9 @@ enum {
  * element alignment (2 bytes for 16-bit operands) is required, else
  * SG_ERR_ALIGN.  C must be aligned to its own elements (4 bytes for fp32, 2
  * for fp16 / bf16) and bias to 4 bytes, else SG_ERR_ALIGN; a C that is not
- * 16-byte aligned or whose pitch is not a multiple of 16 bytes gets masked
- * element stores instead of TMA stores (slower; the same bits).
+ * 16-byte aligned or whose pitch is not a multiple of 16 bytes is written
+ * row by row from the epilogue's staging buffer with ordinary stores masked
+ * to M x N, instead of by TMA stores (slower; the same bits).
  */
 int sg_gemm(int64_t M, int64_t N, int64_t K,
             const void* A, int64_t lda,
@@ -234,7 +235,7 @@ typedef struct {
     int32_t smem_bytes;    /* dynamic shared memory per CTA (modes 4 and 5:
                               with a bias, the biases too) */
     int32_t tmem_columns;  /* tensor-memory columns allocated per CTA */
-    int32_t tma_store;     /* 1: C written by TMA stores, 0: masked stores */
+    int32_t tma_store;     /* 1: C written by TMA stores, 0: by masked row-by-row stores */
     int32_t cluster_m;     /* CTAs per cluster (1 or 2) */
     int32_t pair_mma;      /* 1: the cluster's two CTAs compute one 256-row tile
                               with the paired MMA, each CTA owning 128 rows of
