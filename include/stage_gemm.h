@@ -38,10 +38,18 @@
  *
  * Ownership: the caller owns A, B, C and bias (device memory, e.g. from
  * PyTorch).  The library never frees caller memory.  It allocates, once per
- * device, a 4-byte device status word and keeps host-side caches;
- * sg_gemm_host also creates, once per device, three streams and five events,
- * and allocates one stream-ordered device buffer per call (released on the
- * call's stream).
+ * device, a 4-byte device status word and keeps host-side caches.  Where an
+ * operand or residual has no TMA-legal layout (see Layouts below), a call
+ * also takes one stream-ordered buffer for a copy of it with 16-byte row
+ * pitches, released on the call's stream after the kernel.  sg_gemm_host
+ * also creates, once per device, three streams and five events, and takes
+ * one stream-ordered device buffer per call (released on the call's
+ * stream).  Those buffers come from a memory pool the library creates on
+ * each device on first use; freed blocks stay in it, so a later call maps
+ * no new memory, and the pool keeps up to the largest amount used at once
+ * until the process exits.  While `stream` is being captured into a graph
+ * they come from the device's default pool instead.  sg_gemm_noalloc
+ * allocates nothing.
  *
  * Execution: every call is asynchronous on `stream` (a cudaStream_t passed as
  * void*; NULL is the legacy default stream).  Argument checks run on the
@@ -119,9 +127,12 @@ enum {
  *
  * Layouts: an operand whose base is 16-byte aligned and whose row pitch is
  * a multiple of 16 bytes (lda, ldb multiples of 8 elements, of 16 for FP8;
- * any pitch for a single row) is staged by TMA.  Any other operand is staged by element
- * loads of the producer warp into the same shared-memory layout (slower; the
- * kernel then runs one CTA per tile); the results are bit-identical.  Only
+ * any pitch for a single row) is staged by TMA.  Any other operand (and any
+ * such residual) is first copied on `stream` into a buffer with 16-byte row
+ * pitches and staged from there by TMA; if that buffer cannot be had (and
+ * always in sg_gemm_noalloc) it is staged by element loads of the producer
+ * warp into the same shared-memory layout (slower; the kernel then runs one
+ * CTA per tile).  The results are bit-identical either way.  Only
  * element alignment (2 bytes for 16-bit operands) is required, else
  * SG_ERR_ALIGN.  C must be aligned to its own elements (4 bytes for fp32, 2
  * for fp16 / bf16) and bias to 4 bytes, else SG_ERR_ALIGN; a C that is not
@@ -190,8 +201,8 @@ int sg_gemm_qb(int64_t M, int64_t N, int64_t K,
  * buffers: A, B, R (may be NULL: no residual), bias and C are host pointers
  * with the meanings, layouts and pitches of sg_gemm / sg_gemm_residual.
  * The pages define only the product; this call adds the transfers around
- * it.  It allocates one device buffer (stream-ordered, cudaMallocAsync on
- * `stream`, released with cudaFreeAsync on the same stream), copies bias
+ * it.  It takes one device buffer (stream-ordered, from the library's pool
+ * on `stream`, released with cudaFreeAsync on the same stream), copies bias
  * and B in, then copies A (and R) in row chunks on a library-owned stream
  * while each chunk's GEMM runs as soon as its rows have arrived (chunks
  * alternate between `stream` and a library-owned compute stream, so one
@@ -379,7 +390,9 @@ int sg_version(void);
  * embedding runtime that owns every device allocation (and budgets it), or
  * in a process that must not grow its device footprint after start-up.
  * sg_gemm allocates a 4-byte device status word on its first call on each
- * device; this entry point never does.
+ * device, and a buffer for a copy of any operand without a TMA-legal layout;
+ * this entry point does neither (such an operand is staged by element
+ * loads).
  *
  * Scratch: the kernel's only scratch memory is that status word (written by
  * a device-side wait that gives up).  Here it lives in a file-scope

@@ -59,6 +59,15 @@ int sg_test_set_cluster(int mode);
  */
 int sg_test_set_tail_split(int on);
 
+/*
+ * Whether later sg_gemm / sg_gemm_residual / sg_gemm_ex calls may copy an
+ * operand or residual without a TMA-legal layout into a stream-ordered
+ * buffer with 16-byte pitches (1, the default) or must stage it by element
+ * loads (0, as sg_gemm_noalloc always does).  The copies move values only,
+ * so C must be bit-identical either way.  Returns 0, or SG_ERR_ARG.
+ */
+int sg_test_set_repack(int on);
+
 #ifdef __cplusplus
 }
 #endif

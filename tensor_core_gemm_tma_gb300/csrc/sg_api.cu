@@ -49,6 +49,10 @@ struct DevState {
     // sg_gemm_host: library-owned copy streams, a second compute stream and
     // events, created on first use
     cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
+    // the library's stream-ordered memory pool (scratch_pool), created on first use
+    int dev = 0;
+    bool pool_tried = false;
+    cudaMemPool_t pool = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_in = nullptr, ev_gemm = nullptr, ev_out = nullptr, ev_comp = nullptr;
 };
 
@@ -173,10 +177,51 @@ int device_state(DevState** out) {
         if (int rc = ensure_encode_fn(); rc != SG_OK) return rc;
         if (cudaMalloc(&st.status, sizeof(int)) != cudaSuccess) return SG_ERR_CUDA;
         if (cudaMemset(st.status, 0, sizeof(int)) != cudaSuccess) return SG_ERR_CUDA;
+        st.dev = dev;
         st.ready = true;
     }
     *out = &st;
     return SG_OK;
+}
+
+// The library's stream-ordered memory pool on this device, created on first
+// use.  sg_gemm_host's staging buffer and the 16-byte-pitch copies of
+// operands come from it.  Blocks freed on a stream stay in the pool (no
+// release threshold), so a later call of the same size maps no new memory;
+// the device's default pool, whose threshold is 0, would return them at
+// every synchronisation and map them again on the next call.  The pool and
+// what it holds last until the process exits.
+cudaMemPool_t scratch_pool(DevState& st) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!st.pool_tried) {
+        st.pool_tried = true;
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = st.dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+            uint64_t keep = UINT64_MAX;
+            if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) == cudaSuccess) {
+                st.pool = pool;
+            } else {
+                cudaMemPoolDestroy(pool);
+            }
+        }
+        cudaGetLastError();  // a device without pools: the default pool serves
+    }
+    return st.pool;
+}
+
+// A stream-ordered allocation from the library's pool; from the device's
+// default pool while `s` is being captured into a graph (the allocation then
+// becomes the graph's own) or where the library has no pool.  Freed with
+// cudaFreeAsync either way.
+cudaError_t pool_alloc(DevState& st, void** p, size_t bytes, cudaStream_t s) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return cudaErrorUnknown;
+    cudaMemPool_t pool = cap == cudaStreamCaptureStatusNone ? scratch_pool(st) : nullptr;
+    return pool ? cudaMallocFromPoolAsync(p, bytes, pool, s) : cudaMallocAsync(p, bytes, s);
 }
 
 // The copy streams and events of sg_gemm_host, once per device.
@@ -305,6 +350,10 @@ std::atomic<int> g_tail_split{[] {
     const char* e = std::getenv("STAGE_GEMM_TAIL_SPLIT");
     return (e && std::atoi(e) == 0) ? 0 : 1;
 }()};
+
+// Whether operands without a TMA-legal layout may be copied to 16-byte
+// pitches before the launch (sg_test_set_repack; 1 by default).
+std::atomic<int> g_repack{1};
 
 // Kernel mode forced by sg_test_set_cluster or, at load, the environment
 // variable STAGE_GEMM_CLUSTER (1: single CTA, 3: paired MMA, 4: resident B,
@@ -604,7 +653,7 @@ bool honours(const Plan& pl, const Choice& c) {
 // the entry points; `st` supplies the device's attributes and status word).
 // With Bq (mode 5) B is int8 codes with per-column scales b_scale, decoded
 // into the resident panel; B is then unused.
-int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+int plan_and_launch_impl(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
                     int stages, int64_t skip_load, cudaStream_t stream, const Choice* forced = nullptr,
                     Plan* used = nullptr, const void* R = nullptr, int64_t ldr = 0, const int8_t* Bq = nullptr,
@@ -682,6 +731,64 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     prm.b_scale = b_scale;
     prm.in_bf16 = in_dtype == SG_BF16 ? 1 : 0;
     return launch_plan(st, out_dtype, pl, ta, tb, tc, tr, prm, R != nullptr, stream);
+}
+
+// As plan_and_launch_impl, but an operand or a residual without a TMA-legal
+// layout (a base off a 16-byte boundary or a pitch that is not a multiple of
+// 16 bytes) is first copied, on the stream, into one stream-ordered buffer
+// with 16-byte row pitches, so the kernel stages it by TMA rather than by
+// element loads (on GB300, 100000 x 128 x 500 with a 500-column B: 472 us by
+// element loads, ~40 us copied).  The copies move values only, so C keeps its
+// bits.  Without the buffer (an allocation that fails) the kernel takes the
+// element path.  The allocation-free entry point calls the impl directly.
+int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
+                    int stages, int64_t skip_load, cudaStream_t stream, const Choice* forced = nullptr,
+                    Plan* used = nullptr, const void* R = nullptr, int64_t ldr = 0, const int8_t* Bq = nullptr,
+                    const float* b_scale = nullptr) {
+    const int esz = elem_bytes(in_dtype), oes = elem_bytes(out_dtype);
+    const bool decode = Bq != nullptr;
+    const bool fix_a = K > 0 && !tma_legal(A, M, lda, esz);
+    const bool fix_b = K > 0 && !decode && !tma_legal(B, K, ldb, esz);
+    const bool fix_r = R != nullptr && !c_tma_legal(R, M, ldr, out_dtype);
+    auto direct = [&] {
+        return plan_and_launch_impl(st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                                    skip_load, stream, forced, used, R, ldr, Bq, b_scale);
+    };
+    if ((!fix_a && !fix_b && !fix_r) || !g_repack.load()) return direct();
+    auto pitch16 = [](int64_t cols, int e) { return cdiv(std::max<int64_t>(cols, 1), 16 / e) * (16 / e); };
+    auto up = [](uint64_t b) { return (b + 255) & ~uint64_t(255); };
+    const int64_t pa = fix_a ? pitch16(K, esz) : lda, pb = fix_b ? pitch16(N, esz) : ldb;
+    const int64_t pr = fix_r ? pitch16(N, oes) : ldr;
+    const uint64_t a_bytes = fix_a ? up(uint64_t(M) * pa * esz) : 0, b_bytes = fix_b ? up(uint64_t(K) * pb * esz) : 0;
+    const uint64_t r_bytes = fix_r ? up(uint64_t(M) * pr * oes) : 0;
+    char* buf = nullptr;
+    if (pool_alloc(st, reinterpret_cast<void**>(&buf), a_bytes + b_bytes + r_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();  // no buffer: the element path
+        return direct();
+    }
+    const auto D2D = cudaMemcpyDeviceToDevice;
+    const void* A2 = fix_a ? buf : A;
+    const void* B2 = fix_b ? buf + a_bytes : B;
+    const void* R2 = fix_r ? buf + a_bytes + b_bytes : R;
+    bool ok = true;
+    if (fix_a) ok = cudaMemcpy2DAsync(buf, pa * esz, A, lda * esz, K * esz, M, D2D, stream) == cudaSuccess;
+    if (ok && fix_b)
+        ok = cudaMemcpy2DAsync(buf + a_bytes, pb * esz, B, ldb * esz, N * esz, K, D2D, stream) == cudaSuccess;
+    if (ok && fix_r)
+        ok = cudaMemcpy2DAsync(buf + a_bytes + b_bytes, pr * oes, R, ldr * oes, N * oes, M, D2D, stream) ==
+             cudaSuccess;
+    int rc;
+    if (ok) {
+        rc = plan_and_launch_impl(st, M, N, K, A2, pa, B2, pb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                                  skip_load, stream, forced, used, R2, pr, Bq, b_scale);
+    } else {
+        cudaGetLastError();
+        rc = direct();
+    }
+    // released on the stream, after the kernel that reads it
+    const bool freed = cudaFreeAsync(buf, stream) == cudaSuccess;
+    return (rc == SG_OK && !freed) ? SG_ERR_CUDA : rc;
 }
 
 }  // namespace
@@ -773,7 +880,7 @@ int sg_gemm_host(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, co
 
     std::lock_guard<std::mutex> lk(g_host_mu);
     char* buf = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&buf), total, s) != cudaSuccess) return SG_ERR_CUDA;
+    if (pool_alloc(*st, reinterpret_cast<void**>(&buf), total, s) != cudaSuccess) return SG_ERR_CUDA;
     char* dA = K > 0 ? buf : nullptr;
     char* dB = K > 0 ? buf + a_bytes : nullptr;
     char* dC = buf + a_bytes + b_bytes;
@@ -1091,6 +1198,12 @@ int sg_test_set_tail_split(int on) {
     return SG_OK;
 }
 
+int sg_test_set_repack(int on) {
+    if (on != 0 && on != 1) return SG_ERR_ARG;
+    g_repack.store(on);
+    return SG_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -1151,8 +1264,9 @@ int sg_gemm_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's word: clear it for this call
     if (cudaMemsetAsync(st->status, 0, sizeof(int), s) != cudaSuccess) return SG_ERR_CUDA;
-    return plan_and_launch(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
-                           g_skip_load.load(), s);
+    // the impl: an operand without a TMA-legal layout takes the element path here
+    return plan_and_launch_impl(*st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+                                g_skip_load.load(), s);
 }
 
 int sg_gemm_noalloc_status(void* stream) {

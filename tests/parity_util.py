@@ -4,6 +4,7 @@ the stated bound |C_gpu - C_ref| <= 1e-3 * sum_k |a_ik b_kj| + 1e-5, plus one
 ulp of C_ref for fp16 / bf16 outputs."""
 from __future__ import annotations
 
+import contextlib
 import numpy as np
 
 import gemm_inputs
@@ -111,3 +112,17 @@ def seeded_case(M, N, K, in_dt, seed, dist=("normal", 0.0, 1.0), lda=None, ldb=N
         bp[:, :N] = b
         b = bp
     return a, b
+
+
+@contextlib.contextmanager
+def repack(on):
+    """Within the block, operands (and residuals) without a TMA-legal layout
+    are copied to 16-byte pitches before the launch (on=1, the library's
+    default) or staged by element loads (on=0)."""
+    import tensor_core_gemm_tma_gb300 as sg
+    lib = sg.load_library()
+    assert lib.sg_test_set_repack(int(on)) == 0
+    try:
+        yield
+    finally:
+        lib.sg_test_set_repack(1)

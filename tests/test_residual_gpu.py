@@ -9,7 +9,7 @@ import pytest
 
 import gemm_inputs
 import oracle
-from parity_util import bits_dtype, decode_np, from_device_bits, seeded_case, to_device_bits
+from parity_util import bits_dtype, decode_np, from_device_bits, repack, seeded_case, to_device_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -99,16 +99,19 @@ def test_residual_in_place(out_dt):
 
 @pytest.mark.parametrize("out_dt", ["f16", "f32"])
 def test_residual_element_loads_bit_identical(out_dt):
-    """An R off a 16-byte boundary or with an odd pitch is read by element
-    loads: the same bits as the TMA-staged residual."""
+    """An R off a 16-byte boundary or with an odd pitch, copied to a 16-byte
+    pitch or read by element loads: the same bits as the TMA-staged
+    residual."""
     M, N, K = 260, 136, 192
     a, b = seeded_case(M, N, K, "f16", seed=83)
     r = _rbits(M, N, out_dt, 83)
     tma = run_residual(a, b, r, M, N, K, "f16", out_dt)
-    off = run_residual(a, b, r, M, N, K, "f16", out_dt, r_offset=1)
     r_odd = _rbits(M, N, out_dt, 83, ld=N + 1)
-    odd = run_residual(a, b, r_odd, M, N, K, "f16", out_dt)
-    assert np.array_equal(tma, off) and np.array_equal(tma, odd)
+    for on in (1, 0):  # copied to a 16-byte pitch, then read by element loads
+        with repack(on):
+            off = run_residual(a, b, r, M, N, K, "f16", out_dt, r_offset=1)
+            odd = run_residual(a, b, r_odd, M, N, K, "f16", out_dt)
+        assert np.array_equal(tma, off) and np.array_equal(tma, odd), on
     check(tma, a, b, r, "f16", out_dt, what="tma residual")
 
 

@@ -1,14 +1,16 @@
 """Operands without a TMA-legal layout (a base off a 16-byte boundary, or a
-row pitch that is not a multiple of 16 bytes) are staged by element loads
-of the producer warp into the same swizzled layout, with 0 written where the
-index is out of range (Tolk.Stage: a failing gate copies 0).  Staging moves
-values and never rounds them, so C must be bit-identical to the TMA path on
-the same values, and within the parity bound of the oracle."""
+row pitch that is not a multiple of 16 bytes) are either copied to 16-byte
+pitches before the launch (the device entry points' default) or staged by
+element loads of the producer warp into the same swizzled layout, with 0
+written where the index is out of range (Tolk.Stage: a failing gate copies
+0; sg_gemm_noalloc always takes this path).  Staging moves values and never
+rounds them, so C must be bit-identical between the two and to the TMA path
+on the same values, and within the parity bound of the oracle."""
 import numpy as np
 import pytest
 
 import oracle
-from parity_util import compare, from_device_bits, run_gpu, seeded_case, to_device_bits
+from parity_util import compare, from_device_bits, repack, run_gpu, seeded_case, to_device_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +25,11 @@ def _lib():
 def test_dense_odd_pitches(M, N, K):
     """Dense row-major operands whose pitch (K or N elements) breaks the TMA rule."""
     a, b = seeded_case(M, N, K, "f16", seed=M + N + K)
-    got = run_gpu(a, b, M, N, K, "f16", "f32", "relu")
+    with repack(1):
+        got = run_gpu(a, b, M, N, K, "f16", "f32", "relu")
+    with repack(0):
+        elem = run_gpu(a, b, M, N, K, "f16", "f32", "relu")
+    assert np.array_equal(got, elem)
     ref, _, S = oracle.gemm(a, b, "f16", "f32", "relu")
     compare(got, ref, S, "f32", f"dense {M}x{N}x{K}")
 
@@ -58,11 +64,13 @@ def test_offset_views_bit_identical_to_tma(in_dt):
     A2 = to_device_bits(a_off, in_dt, dev)
     B2 = to_device_bits(b_off, in_dt, dev)
     for which in ("A", "B", "AB"):
-        C = torch.empty(M, N, dtype=torch.float32, device=dev)
-        ap, lda = (A2.data_ptr() + 2, K + 8) if "A" in which else (A.data_ptr(), K)
-        bp, ldb = (B2.data_ptr() + 2, N + 8) if "B" in which else (B.data_ptr(), N)
-        _raw(ap, lda, bp, ldb, M, N, K, in_dt, "f32", C)
-        assert torch.equal(C.view(torch.int32), C_tma.view(torch.int32)), which
+        for on in (1, 0):  # copied to 16-byte pitches, then staged by element loads
+            C = torch.empty(M, N, dtype=torch.float32, device=dev)
+            ap, lda = (A2.data_ptr() + 2, K + 8) if "A" in which else (A.data_ptr(), K)
+            bp, ldb = (B2.data_ptr() + 2, N + 8) if "B" in which else (B.data_ptr(), N)
+            with repack(on):
+                _raw(ap, lda, bp, ldb, M, N, K, in_dt, "f32", C)
+            assert torch.equal(C.view(torch.int32), C_tma.view(torch.int32)), (which, on)
     ref, _, S = oracle.gemm(a, b, in_dt, "f32")
     compare(from_device_bits(C_tma, "f32"), ref, S, "f32", "tma")
 
@@ -71,7 +79,10 @@ def test_element_path_stage_counts_bit_identical():
     import torch
     M, N, K = 300, 200, 333
     a, b = seeded_case(M, N, K, "bf16", seed=52)
-    outs = [run_gpu(a, b, M, N, K, "bf16", "bf16", stages=s) for s in (1, 2, 3, 6)]
+    with repack(0):
+        outs = [run_gpu(a, b, M, N, K, "bf16", "bf16", stages=s) for s in (1, 2, 3, 6)]
+    with repack(1):
+        outs.append(run_gpu(a, b, M, N, K, "bf16", "bf16"))
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
     ref, _, S = oracle.gemm(a, b, "bf16", "bf16")
@@ -82,7 +93,11 @@ def test_element_path_nan_padding_never_read():
     """Odd pitch plus NaN in the padding: the padding must not be read."""
     M, N, K = 140, 90, 70
     a, b = seeded_case(M, N, K, "f16", seed=53, lda=73, ldb=93)
-    got = run_gpu(a, b, M, N, K, "f16", "f16", "bias_relu", np.linspace(-1, 1, N).astype(np.float32))
+    with repack(0):
+        got = run_gpu(a, b, M, N, K, "f16", "f16", "bias_relu", np.linspace(-1, 1, N).astype(np.float32))
+    with repack(1):
+        copied = run_gpu(a, b, M, N, K, "f16", "f16", "bias_relu", np.linspace(-1, 1, N).astype(np.float32))
+    assert np.array_equal(got, copied)
     assert np.all(np.isfinite(got.view(np.float16)))
     ref, _, S = oracle.gemm(a, b, "f16", "f16", "bias_relu", np.linspace(-1, 1, N).astype(np.float32), K=K, N=N)
     compare(got, ref, S, "f16", "element nan padding")
