@@ -737,10 +737,12 @@ int plan_and_launch_impl(DevState& st, int64_t M, int64_t N, int64_t K, const vo
 // layout (a base off a 16-byte boundary or a pitch that is not a multiple of
 // 16 bytes) is first copied, on the stream, into one stream-ordered buffer
 // with 16-byte row pitches, so the kernel stages it by TMA rather than by
-// element loads (on GB300, 100000 x 128 x 500 with a 500-column B: 472 us by
-// element loads, ~40 us copied).  The copies move values only, so C keeps its
-// bits.  Without the buffer (an allocation that fails) the kernel takes the
-// element path.  The allocation-free entry point calls the impl directly.
+// element loads (on GB300, 100000 x 128 x 500 with a 500-column B: 475 us by
+// element loads, 48 us copied); such a C is computed into the buffer and its
+// N columns copied out row by row afterwards (its padding is not written).
+// The copies move values only, so C keeps its bits.  Without the buffer (an
+// allocation that fails) the kernel takes the element paths.  The
+// allocation-free entry point calls the impl directly.
 int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, void* C, int64_t ldc, int in_dtype, int out_dtype, int epilogue, const float* bias,
                     int stages, int64_t skip_load, cudaStream_t stream, const Choice* forced = nullptr,
@@ -751,19 +753,20 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     const bool fix_a = K > 0 && !tma_legal(A, M, lda, esz);
     const bool fix_b = K > 0 && !decode && !tma_legal(B, K, ldb, esz);
     const bool fix_r = R != nullptr && !c_tma_legal(R, M, ldr, out_dtype);
+    const bool fix_c = !c_tma_legal(C, M, ldc, out_dtype);
     auto direct = [&] {
         return plan_and_launch_impl(st, M, N, K, A, lda, B, ldb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
                                     skip_load, stream, forced, used, R, ldr, Bq, b_scale);
     };
-    if ((!fix_a && !fix_b && !fix_r) || !g_repack.load()) return direct();
+    if ((!fix_a && !fix_b && !fix_r && !fix_c) || !g_repack.load()) return direct();
     auto pitch16 = [](int64_t cols, int e) { return cdiv(std::max<int64_t>(cols, 1), 16 / e) * (16 / e); };
     auto up = [](uint64_t b) { return (b + 255) & ~uint64_t(255); };
     const int64_t pa = fix_a ? pitch16(K, esz) : lda, pb = fix_b ? pitch16(N, esz) : ldb;
-    const int64_t pr = fix_r ? pitch16(N, oes) : ldr;
+    const int64_t pr = fix_r ? pitch16(N, oes) : ldr, pc = fix_c ? pitch16(N, oes) : ldc;
     const uint64_t a_bytes = fix_a ? up(uint64_t(M) * pa * esz) : 0, b_bytes = fix_b ? up(uint64_t(K) * pb * esz) : 0;
-    const uint64_t r_bytes = fix_r ? up(uint64_t(M) * pr * oes) : 0;
+    const uint64_t r_bytes = fix_r ? up(uint64_t(M) * pr * oes) : 0, c_bytes = fix_c ? up(uint64_t(M) * pc * oes) : 0;
     char* buf = nullptr;
-    if (pool_alloc(st, reinterpret_cast<void**>(&buf), a_bytes + b_bytes + r_bytes, stream) != cudaSuccess) {
+    if (pool_alloc(st, reinterpret_cast<void**>(&buf), a_bytes + b_bytes + r_bytes + c_bytes, stream) != cudaSuccess) {
         cudaGetLastError();  // no buffer: the element path
         return direct();
     }
@@ -771,6 +774,7 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
     const void* A2 = fix_a ? buf : A;
     const void* B2 = fix_b ? buf + a_bytes : B;
     const void* R2 = fix_r ? buf + a_bytes + b_bytes : R;
+    void* C2 = fix_c ? buf + a_bytes + b_bytes + r_bytes : C;
     bool ok = true;
     if (fix_a) ok = cudaMemcpy2DAsync(buf, pa * esz, A, lda * esz, K * esz, M, D2D, stream) == cudaSuccess;
     if (ok && fix_b)
@@ -780,8 +784,11 @@ int plan_and_launch(DevState& st, int64_t M, int64_t N, int64_t K, const void* A
              cudaSuccess;
     int rc;
     if (ok) {
-        rc = plan_and_launch_impl(st, M, N, K, A2, pa, B2, pb, C, ldc, in_dtype, out_dtype, epilogue, bias, stages,
+        rc = plan_and_launch_impl(st, M, N, K, A2, pa, B2, pb, C2, pc, in_dtype, out_dtype, epilogue, bias, stages,
                                   skip_load, stream, forced, used, R2, pr, Bq, b_scale);
+        if (rc == SG_OK && fix_c &&
+            cudaMemcpy2DAsync(C, ldc * oes, C2, pc * oes, N * oes, M, D2D, stream) != cudaSuccess)
+            rc = SG_ERR_CUDA;
     } else {
         cudaGetLastError();
         rc = direct();

@@ -106,17 +106,20 @@ def test_element_path_nan_padding_never_read():
 @pytest.mark.parametrize("out_dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("epi", ["none", "relu", "bias_relu"])
 def test_c_without_tma_layout_bit_identical(out_dt, epi):
-    """A C whose pitch breaks the TMA rule (N + 1 elements) is written row by
-    row from the staging buffer: the same bits as the TMA store of a dense C,
-    nothing past N or M written (a canary fills the padding column), for
-    ragged M and N."""
+    """A C whose pitch breaks the TMA rule (N + 1 elements) is computed into a
+    16-byte-pitch buffer and copied out (the default), or written row by row
+    from the staging buffer (element path): either way the same bits as the
+    TMA store of a dense C, nothing past N or M written (a canary fills the
+    padding column), for ragged M and N."""
     M, N, K = 333, 200, 96
     a, b = seeded_case(M, N, K, "f16", seed=54)
     bias = np.linspace(-1, 1, N).astype(np.float32) if epi == "bias_relu" else None
     dense = run_gpu(a, b, M, N, K, "f16", out_dt, epi, bias)
     canary = 0x7F7F7F7F if out_dt == "f32" else 0x7E7E
-    odd = run_gpu(a, b, M, N, K, "f16", out_dt, epi, bias, ldc=N + 1, canary=canary)
-    assert np.array_equal(odd[:, :N], dense)
-    assert np.all(odd[:, N] == canary)
+    for on in (1, 0):
+        with repack(on):
+            odd = run_gpu(a, b, M, N, K, "f16", out_dt, epi, bias, ldc=N + 1, canary=canary)
+        assert np.array_equal(odd[:, :N], dense), on
+        assert np.all(odd[:, N] == canary), on
     ref, _, S = oracle.gemm(a, b, "f16", out_dt, epi, bias, K=K, N=N)
     compare(odd[:, :N], ref, S, out_dt, f"element-stored C {out_dt} {epi}")
