@@ -136,9 +136,11 @@ enum {
  * element alignment (2 bytes for 16-bit operands) is required, else
  * SG_ERR_ALIGN.  C must be aligned to its own elements (4 bytes for fp32, 2
  * for fp16 / bf16) and bias to 4 bytes, else SG_ERR_ALIGN; a C that is not
- * 16-byte aligned or whose pitch is not a multiple of 16 bytes is written
- * row by row from the epilogue's staging buffer with ordinary stores masked
- * to M x N, instead of by TMA stores (slower; the same bits).
+ * 16-byte aligned or whose pitch is not a multiple of 16 bytes is computed
+ * into a buffer with 16-byte row pitches and its N columns copied into
+ * place on `stream` (its padding is not written); without that buffer (and
+ * in sg_gemm_noalloc) it is written row by row from the epilogue's staging
+ * buffer with ordinary stores masked to M x N.  The same bits either way.
  */
 int sg_gemm(int64_t M, int64_t N, int64_t K,
             const void* A, int64_t lda,
