@@ -248,7 +248,10 @@ typedef struct {
     int32_t smem_bytes;    /* dynamic shared memory per CTA (modes 4 and 5:
                               with a bias, the biases too) */
     int32_t tmem_columns;  /* tensor-memory columns allocated per CTA */
-    int32_t tma_store;     /* 1: C written by TMA stores, 0: by masked row-by-row stores */
+    int32_t tma_store;     /* 1: C written by TMA stores; 0: C has no
+                              TMA-legal layout (sg_gemm computes it into a
+                              16-byte-pitch buffer and copies it into place,
+                              sg_gemm_noalloc writes it row by row) */
     int32_t cluster_m;     /* CTAs per cluster (1 or 2) */
     int32_t pair_mma;      /* 1: the cluster's two CTAs compute one 256-row tile
                               with the paired MMA, each CTA owning 128 rows of
