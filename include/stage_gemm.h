@@ -184,8 +184,10 @@ int sg_gemm_residual(int64_t M, int64_t N, int64_t K,
  * memory as 16-bit values equal to the codes (exact), every row tile's MMAs
  * read that panel, and s_j multiplies column j of the fp32 accumulator
  * before the bias and the ReLU.  B must fit the resident panel: K <= 128
- * and N <= 512 (else SG_ERR_ARG), and A must be TMA-legal (16-byte aligned
- * base, pitch a multiple of 16 bytes; else SG_ERR_ARG).  The scales must be
+ * and N <= 512 (else SG_ERR_ARG).  A is staged by TMA: an A without a
+ * TMA-legal layout (16-byte aligned base, pitch a multiple of 16 bytes) is
+ * first copied to 16-byte pitches on `stream` (if that copy's buffer cannot
+ * be had, SG_ERR_ARG), and a C likewise as for sg_gemm.  The scales must be
  * finite.  C must not overlap A, Bq, b_scale or bias (SG_ERR_ALIAS); a NULL
  * b_scale, or a NULL Bq with K > 0, is SG_ERR_ARG; a b_scale not aligned
  * to 4 bytes is SG_ERR_ALIGN; in_dtype other than

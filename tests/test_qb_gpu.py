@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import oracle
-from parity_util import compare, from_device_bits, seeded_case, to_device_bits, torch_dtype
+from parity_util import compare, from_device_bits, repack, seeded_case, to_device_bits, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,8 @@ CASES = [
 
 @pytest.mark.parametrize("M,N,K,ind,outd,epi", CASES)
 def test_parity_with_oracle(M, N, K, ind, outd, epi):
-    # A's pitch padded (NaN, never read) to a whole number of 16 bytes: mode 5 stages A by TMA only
+    # A's pitch padded (NaN, never read) to a whole number of 16 bytes: mode 5 stages A by TMA (an odd pitch
+    # would be copied to one first)
     a, _ = seeded_case(M, 1, K, ind, seed=70 + M % 13, lda=-(-K // 8) * 8)
     q, s = _codes(K, N, seed=K + N)
     bias = np.linspace(-0.5, 0.5, N).astype(np.float32) if epi == "bias_relu" else None
@@ -141,8 +142,17 @@ def test_panel_limits_and_types_rejected():
     A = torch.zeros((256, 256), dtype=torch.float16, device="cuda")
     S = torch.ones(600, dtype=torch.float32, device="cuda")
     Q = torch.zeros((64, 64), dtype=torch.int8, device="cuda")
-    with pytest.raises(sg.SgError) as e:           # A's pitch (100 halves) not a whole number of 16 bytes
-        sg.stage_gemm_qb(torch.zeros((256, 100), dtype=torch.float16, device="cuda")[:, :64], Q, S[:64])
+    # A's pitch (100 halves) is not a whole number of 16 bytes: it is copied to a 16-byte pitch first and gives
+    # the bits of a dense A; staged by element loads instead (the copy switched off) the decoded panel cannot
+    # take it
+    A_odd = torch.randn((256, 100), device="cuda").half()[:, :64]
+    Qr = torch.randint(-8, 8, (64, 64), dtype=torch.int8, device="cuda")
+    with repack(1):
+        got = sg.stage_gemm_qb(A_odd, Qr, S[:64])
+    assert torch.equal(got, sg.stage_gemm_qb(A_odd.contiguous(), Qr, S[:64]))
+    with repack(0):
+        with pytest.raises(sg.SgError) as e:
+            sg.stage_gemm_qb(A_odd, Q, S[:64])
     assert e.value.code == -1
     for K, N in ((136, 128), (128, 520)):      # past 2 K chunks / 4 column blocks
         Q = torch.zeros((K, N), dtype=torch.int8, device="cuda")
